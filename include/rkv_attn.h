@@ -1,0 +1,167 @@
+/*
+ * rkv_attn.h -- C ABI of the GB300 resident-attention library (librkv_attn.so).
+ *
+ * Three operations on GPU-resident f32 data, computing
+ *     output = softmax(Q . K^T * scale) . V          per query head
+ * as defined on the trueno-gpu 0.4.11 page (src/memory/resident/attention.rs,
+ * fn batched_multihead_attention: the doc comment's softmax(Q K^T / sqrt(d_k)) V)
+ * and the trustformers-core 0.2.0 page (src/gpu_ops/cuda/oxicuda/attention.rs,
+ * fn attention_prefill_gpu_to_gpu / fn attention_decode_gpu_to_gpu).
+ *
+ * Conventions shared by every entry point
+ *  - Every tensor pointer is a DEVICE pointer to row-major float32 (int32 for
+ *    lengths), 16-byte aligned.  The caller owns all memory; the library
+ *    allocates nothing, copies nothing to the host and never synchronises.
+ *  - Work is enqueued on `stream` and the call returns at once (the pages'
+ *    "no sync, caller chains on its stream" convention: trueno-gpu,
+ *    fn incremental_attention_gpu_with_stream / fn kv_cache_scatter_gpu).
+ *  - Shapes are validated on the host before anything is launched
+ *    (the pages' InvalidParameter / shape_error pattern); a rejected call
+ *    launches nothing and returns RKV_ERR_INVALID_ARG or RKV_ERR_UNSUPPORTED,
+ *    with a message in rkv_last_error().
+ *  - Values that live in device memory (lengths, positions) cannot be checked
+ *    on the host without a sync; kernels clamp or skip them and record the
+ *    event in a device flag word read by rkv_read_device_flags().
+ *  - GQA: query head h uses kv head h / (n_heads / n_kv_heads); n_heads must
+ *    be a multiple of n_kv_heads (realizar 0.8.5, cache_from_cache_from_kv_cache.rs,
+ *    fn init_kv_cache_gpu sizes the cache by num_kv_heads <= num_heads).
+ *  - head_dim must be one of 16, 32, 64, 128 (RKV_ERR_UNSUPPORTED otherwise).
+ *  - scale == 0 selects 1/sqrt(head_dim) (trueno-gpu,
+ *    fn batched_multihead_attention); a negative or non-finite scale is
+ *    rejected.
+ *  - Zero-sized work (batch, seq_len, M or T == 0) is a successful no-op.
+ */
+#ifndef RKV_ATTN_H
+#define RKV_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if !defined(__DRIVER_TYPES_H__)
+typedef struct CUstream_st* cudaStream_t;   /* same type as the CUDA runtime's */
+#endif
+
+typedef enum {
+    RKV_OK = 0,
+    RKV_ERR_INVALID_ARG = 1,   /* bad pointer, shape, alignment or workspace */
+    RKV_ERR_UNSUPPORTED = 2,   /* valid request outside what the kernels implement */
+    RKV_ERR_LAUNCH = 3,        /* the CUDA runtime reported an error */
+    RKV_ERR_DEVICE = 4         /* a device-side condition, see rkv_read_device_flags */
+} rkv_status;
+
+/* Device flag bits (rkv_read_device_flags). */
+#define RKV_FLAG_WAIT_TIMEOUT    0x1u  /* a bounded on-chip wait gave up; outputs invalid */
+#define RKV_FLAG_LEN_CLAMPED     0x2u  /* a seq_lens entry exceeded its bound and was clamped */
+#define RKV_FLAG_NEGATIVE_INPUT  0x4u  /* a negative length or position was treated as 0 / skipped */
+
+/* Library version, (major << 16) | minor. */
+int rkv_version(void);
+
+/* Static text for a status code. */
+const char* rkv_status_string(rkv_status status);
+
+/* Message describing the most recent failing call made on this host thread
+ * ("" if none).  The pointer stays valid until the next call on this thread. */
+const char* rkv_last_error(void);
+
+/*
+ * Reads (and, if clear != 0, resets) the device flag word of the current
+ * device.  Synchronises `stream`.  Returns RKV_OK and *flags, or
+ * RKV_ERR_LAUNCH.  Diagnostic only; the compute entry points never sync.
+ */
+rkv_status rkv_read_device_flags(unsigned int* flags, int clear, cudaStream_t stream);
+
+/*
+ * Prefill attention over interleaved activations, causal or not, with GQA.
+ *
+ * Cites: trueno-gpu attention.rs, fn batched_multihead_attention_optimized
+ * (interleaved [seq, n_heads*head_dim] in and out); trustformers-core
+ * attention.rs, fn attention_prefill_gpu_to_gpu (causal: query i sees keys
+ * 0..=i, from an empty cache).
+ *
+ *   q        [batch, seq_len, n_heads*head_dim]      input
+ *   k, v     [batch, seq_len, n_kv_heads*head_dim]   input
+ *   o        [batch, seq_len, n_heads*head_dim]      output, fully written
+ *   causal   0: every query sees keys 0..len-1; 1: query i sees keys 0..min(i, len-1)
+ *   seq_lens device int32[batch] valid lengths (<= seq_len), or NULL for all
+ *            seq_len.  Query rows i >= len are written as 0; keys j >= len are
+ *            ignored.  Entries > seq_len are clamped (RKV_FLAG_LEN_CLAMPED),
+ *            negative entries count as 0 (RKV_FLAG_NEGATIVE_INPUT).
+ *   scale    0 -> 1/sqrt(head_dim)
+ * Heads are read in place (no head-split copies); no score matrix is stored.
+ * Arithmetic: QK^T and PV on TF32 tensor cores with f32 accumulation; softmax
+ * in f32.  o must not alias q, k or v.
+ */
+rkv_status attn_prefill(const float* q, const float* k, const float* v, float* o,
+                        int batch, int seq_len, int n_heads, int n_kv_heads, int head_dim,
+                        int causal, const int* seq_lens, float scale, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace attn_decode_batched needs for these sizes.
+ * Returns 0 for invalid sizes.
+ */
+size_t attn_decode_workspace_bytes(int M, int n_heads, int n_kv_heads, int head_dim,
+                                   int max_len);
+
+/*
+ * Batched single-token decode attention against the resident KV cache.
+ *
+ * Cites: trueno-gpu attention.rs, fn incremental_attention_gpu (one query per
+ * head against cache rows 0..seq_len-1; seq_len == 0 gives a zero row);
+ * trustformers-core attention.rs, fn attention_decode_gpu_to_gpu (no mask);
+ * realizar cache_from_cache_from_kv_cache.rs, fn init_batched_kv_cache_gpu
+ * (M <= 32 sequences, cache [M, num_kv_heads, max_len, head_dim], per-sequence
+ * lengths).
+ *
+ *   q          [M, n_heads*head_dim]               input, one token per sequence
+ *   k_cache,
+ *   v_cache    [M, n_kv_heads, max_len, head_dim]  input
+ *   o          [M, n_heads*head_dim]               output, fully written
+ *   seq_lens   device int32[M]: rows 0..len-1 of each sequence are attended
+ *              (the length INCLUDING the token just appended).  len > max_len
+ *              is clamped (RKV_FLAG_LEN_CLAMPED); len <= 0 gives a zero row.
+ *   workspace  device buffer of >= attn_decode_workspace_bytes(...) bytes,
+ *              256-byte aligned, ZERO-FILLED before its first use; every call
+ *              leaves the parts that must start at zero zeroed again, so it can
+ *              be reused without clearing.  Calls sharing one workspace must
+ *              not overlap on the GPU (use one workspace per concurrent stream).
+ * 1 <= M <= 32; n_heads / n_kv_heads in {1, 2, 4, 8}.  Split-KV: the cache rows
+ * of all sequences are cut into equal contiguous pieces, one per CTA; pieces
+ * of one (sequence, kv head) are merged with a log-sum-exp combine inside the
+ * same launch.  Arithmetic is f32.
+ */
+rkv_status attn_decode_batched(const float* q, const float* k_cache, const float* v_cache,
+                               float* o, int M, int n_heads, int n_kv_heads, int head_dim,
+                               int max_len, const int* seq_lens, float scale,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Appends T new K/V rows per sequence into the resident cache.
+ *
+ * Cites: trueno-gpu attention.rs, fn kv_cache_scatter_gpu (interleaved
+ * [n_heads*head_dim] row -> cache[head, pos, :], position must be below
+ * max_seq_len); batched layout from realizar fn init_batched_kv_cache_gpu.
+ *
+ *   k_new, v_new      [M, T, n_kv_heads*head_dim]        input
+ *   k_cache, v_cache  [M, n_kv_heads, max_len, head_dim] updated in place:
+ *       cache[m, kh, start_pos[m] + t, :] = new[m, t, kh*head_dim : (kh+1)*head_dim]
+ *   start_pos  device int32[M]
+ *   overflow   device int32*, or NULL.  Tokens whose target row is outside
+ *              [0, max_len) are skipped and each is added once to *overflow
+ *              (the page's host-side pos < max_seq_len check, moved on chip
+ *              because positions live in device memory).
+ * Bit-exact copy; rows not targeted are untouched.  1 <= M <= 32, T <= max_len.
+ */
+rkv_status kv_cache_scatter(const float* k_new, const float* v_new, float* k_cache,
+                            float* v_cache, int M, int T, int n_kv_heads, int head_dim,
+                            int max_len, const int* start_pos, int* overflow,
+                            cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RKV_ATTN_H */

@@ -1,0 +1,484 @@
+// decode_splitkv.cu -- batched single-token decode attention, split-KV, HBM-bound.
+//
+// Semantics: trueno-gpu 0.4.11 src/memory/resident/attention.rs,
+// fn incremental_attention_gpu (one query per head against cache rows
+// 0..seq_len-1, zero row for seq_len == 0) and trustformers-core 0.2.0
+// src/gpu_ops/cuda/oxicuda/attention.rs, fn attention_decode_gpu_to_gpu (no
+// mask), over the batched cache [M, n_kv_heads, max_len, head_dim] of realizar
+// 0.8.5 cache_from_cache_from_kv_cache.rs, fn init_batched_kv_cache_gpu.
+//
+// Design (the pages launch one warp per head, which leaves a 152-SM GPU idle):
+//  * A "segment" is the run of valid cache rows of one (sequence m, kv head kh):
+//    L_m contiguous rows of D floats.  All segments laid end to end form R rows.
+//  * One persistent CTA per SM takes an equal contiguous share of the R rows
+//    (balanced to one row whatever the length mix); the share may cross
+//    segment boundaries, and each part of a segment in one CTA is a "piece".
+//  * A producer warp streams 64-row tiles of K and V with bulk async copies
+//    into a 3-stage shared-memory ring (mbarrier full/empty pairs).
+//  * Eight consumer warps each take 8 rows of a tile.  GQA: the G = H/Hk query
+//    heads that share a kv head are processed together, so every cache row is
+//    read from HBM once per kv head.  Dot products are split over D/4 lanes and
+//    reduced with a transposing butterfly (one shuffle per partial, not one per
+//    head per step); the softmax is online in base 2 with the scale folded into q.
+//  * Each piece ends with (m, l, o) per head.  A piece that is a whole segment
+//    writes the output directly; otherwise it writes a partial record to the
+//    workspace, and the last CTA to finish a segment (atomic ticket) merges the
+//    records with the log-sum-exp rule and resets the ticket to zero.
+#include "rkv_internal.cuh"
+#include "rkv_launch.h"
+
+namespace rkv {
+
+constexpr int kDecConsumerWarps = 8;
+constexpr int kDecThreads = (kDecConsumerWarps + 1) * 32;
+constexpr int kDecConsumerThreads = kDecConsumerWarps * 32;
+constexpr int kDecBatchRows = 8;                                   // rows per warp per tile
+constexpr int kDecTileRows = kDecBatchRows * kDecConsumerWarps;    // 64
+constexpr int kDecMaxCtas = 1024;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__host__ __device__ constexpr int ilog2c(int x) { return x <= 1 ? 0 : 1 + ilog2c(x / 2); }
+
+template <int D, int G>
+struct DecCfg {
+    static constexpr int LPR = D / 4;                 // lanes per cache row (one float4 each)
+    static constexpr int RPW = 32 / LPR;              // rows a warp covers per pass
+    static constexpr int PASSES = kDecBatchRows / RPW;
+    static constexpr int NV = PASSES * G;             // partial dot products per lane
+    static constexpr int NVR = NV >= LPR ? NV / LPR : 1;   // totals per lane after the butterfly
+    static constexpr int ENTRIES = kDecBatchRows * G; // scores per warp per tile
+    static constexpr int EPL = ENTRIES >= 32 ? ENTRIES / 32 : 1;
+    static constexpr int NST = (D == 128) ? (G == 8 ? 2 : 3) : 4;  // pipeline stages
+    static constexpr int REC = ((G * D + 2 * G) + 3) / 4 * 4;      // floats per partial record
+    // shared memory layout (bytes)
+    static constexpr int TILE_BYTES = kDecTileRows * D * 4;
+    static constexpr int OFF_STAGES = 0;
+    static constexpr int OFF_SC = OFF_STAGES + NST * 2 * TILE_BYTES;
+    static constexpr int OFF_RED_ACC = OFF_SC + kDecConsumerWarps * ENTRIES * 4;
+    static constexpr int OFF_RED_ML = OFF_RED_ACC + kDecConsumerWarps * G * D * 4;
+    static constexpr int OFF_P = OFF_RED_ML + kDecConsumerWarps * 2 * G * 4;      // int64 P[33]
+    static constexpr int OFF_L = OFF_P + 34 * 8;                                  // int L[32]
+    static constexpr int OFF_BAR = OFF_L + 32 * 4;                                // full/empty
+    static constexpr int OFF_MISC = OFF_BAR + 2 * NST * 8;                        // abort, last
+    static constexpr int SMEM = OFF_MISC + 16;
+    static_assert(SMEM <= 227 * 1024, "decode shared memory budget");
+    static_assert(NV >= 1 && (LPR & (LPR - 1)) == 0, "lane split");
+};
+
+// Sum NV per-lane values across W lanes (W a power of two): halving exchanges
+// leave each lane the totals of a distinct slice of indices, then plain
+// butterflies finish when fewer values than lanes remain.  After it, a lane
+// holds v[0..NVR) = totals of indices (lane % W) * (NV / W) + t when NV >= W,
+// or v[0] = total of index (lane % W) / (W / NV) when NV < W.
+template <int NV, int W>
+__device__ __forceinline__ void xpose_reduce(float (&v)[NV], int lane) {
+    constexpr int HSTEPS = ilog2c(NV) < ilog2c(W) ? ilog2c(NV) : ilog2c(W);
+#pragma unroll
+    for (int s = 0; s < HSTEPS; ++s) {
+        const int o = (W >> 1) >> s;
+        const int half = (NV >> s) >> 1;
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = up ? v[i] : v[i + half];
+            const float keep = up ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    constexpr int C = NV >> HSTEPS;
+#pragma unroll
+    for (int o = (W >> 1) >> HSTEPS; o >= 1; o >>= 1) {
+#pragma unroll
+        for (int i = 0; i < C; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+    }
+}
+
+// Owner CTA of flat row `pos` when R rows are cut into n shares
+// [floor(R*c/n), floor(R*(c+1)/n)).
+__device__ __forceinline__ int owner_of(int64_t pos, int64_t R, int n) {
+    const int64_t c = ((pos + 1) * (int64_t)n - 1) / R;
+    return c < n - 1 ? (int)c : n - 1;
+}
+
+// First flat row of CTA c's share.
+__device__ __forceinline__ int64_t share_begin(int c, int64_t R, int n) { return R * c / n; }
+
+// Segment containing flat row pos: sequence m (P[m] <= pos < P[m+1]) and kv head.
+__device__ __forceinline__ void locate(int64_t pos, const int64_t* P, const int* L, int Hk, int& m, int& kh,
+                                       int64_t& seg_start) {
+    m = 0;
+    while (P[m + 1] <= pos) ++m;
+    kh = (int)((pos - P[m]) / L[m]);
+    seg_start = P[m] + (int64_t)kh * L[m];
+    (void)Hk;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kDecThreads, 1)
+decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_cache,
+                      const float* __restrict__ v_cache, float* __restrict__ out, int M, int Hk, int Lmax,
+                      const int* __restrict__ seq_lens, float scale_log2, int* __restrict__ tickets,
+                      float* __restrict__ records, unsigned int* __restrict__ flags) {
+    using C = DecCfg<D, G>;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    float* sc_all = reinterpret_cast<float*>(smem + C::OFF_SC);
+    float* red_acc = reinterpret_cast<float*>(smem + C::OFF_RED_ACC);
+    float* red_ml = reinterpret_cast<float*>(smem + C::OFF_RED_ML);
+    int64_t* P = reinterpret_cast<int64_t*>(smem + C::OFF_P);
+    int* L = reinterpret_cast<int*>(smem + C::OFF_L);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int n = gridDim.x;
+    const int c = blockIdx.x;
+    const int H = Hk * G;
+
+    // ---- prologue: lengths, prefix sums, barriers
+    if (warp == 0) {
+        int len = 0;
+        if (lane < M) {
+            len = __ldg(seq_lens + lane);
+            if (len > Lmax) { len = Lmax; atomicOr(flags, RKV_FLAG_LEN_CLAMPED); }
+            if (len < 0) { len = 0; atomicOr(flags, RKV_FLAG_NEGATIVE_INPUT); }
+            L[lane] = len;
+        }
+        int64_t rows = (int64_t)len * Hk, incl = rows;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane < M) P[lane + 1] = incl;
+        if (lane == 0) { P[0] = 0; *abort_flag = 0; *last_flag = 0; }
+    }
+    if (threadIdx.x == 32) {
+        for (int s = 0; s < C::NST; ++s) {
+            mbar_init(smem_addr(&bars[s]), 1);                          // full: producer arrival + tx
+            mbar_init(smem_addr(&bars[C::NST + s]), kDecConsumerWarps);  // empty: one per consumer warp
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    const int64_t R = P[M];
+    const int64_t r0 = share_begin(c, R, n), r1 = share_begin(c + 1, R, n);
+
+    if (warp == kDecConsumerWarps) {
+        // ================================================================ producer
+        if (lane == 0) {
+            int issued[C::NST > 0 ? C::NST : 1];
+            for (int s = 0; s < C::NST; ++s) issued[s] = 0;
+            int it = 0;
+            bool ok = true;
+            int64_t pos = r0;
+            while (ok && pos < r1) {
+                int m, kh;
+                int64_t seg_start;
+                locate(pos, P, L, Hk, m, kh, seg_start);
+                const int64_t piece_end = min(r1, seg_start + L[m]);
+                const int64_t head_row0 = ((int64_t)m * Hk + kh) * Lmax - seg_start;  // flat -> cache row
+                for (int64_t t0 = pos; t0 < piece_end; t0 += kDecTileRows, ++it) {
+                    const int s = it % C::NST;
+                    const uint32_t ph = (uint32_t)(it / C::NST) & 1u;
+                    if (!mbar_wait(smem_addr(&bars[C::NST + s]), ph ^ 1u, abort_flag, flags)) { ok = false; break; }
+                    const int rows = (int)min((int64_t)kDecTileRows, piece_end - t0);
+                    const uint32_t bytes = (uint32_t)rows * D * 4;
+                    const uint32_t full = smem_addr(&bars[s]);
+                    mbar_arrive_expect_tx(full, 2 * bytes);
+                    const int64_t src = (head_row0 + t0) * D;
+                    bulk_g2s(smem_addr(smem + C::OFF_STAGES + (2 * s) * C::TILE_BYTES), k_cache + src, bytes, full);
+                    bulk_g2s(smem_addr(smem + C::OFF_STAGES + (2 * s + 1) * C::TILE_BYTES), v_cache + src, bytes, full);
+                    issued[s] = it + 1;
+                }
+                pos = piece_end;
+            }
+            if (!ok) {   // unwinding: let copies already issued land before the CTA exits
+                for (int s = 0; s < C::NST; ++s)
+                    if (issued[s] > 0)
+                        mbar_drain(smem_addr(&bars[s]), (uint32_t)((issued[s] - 1) / C::NST) & 1u, 100000000ull);
+            }
+        }
+        return;
+    }
+
+    // ==================================================================== consumers
+    // Zero rows for empty sequences (no rows in the partition covers them).
+    for (int sg = c; sg < M * Hk; sg += n) {
+        const int m = sg / Hk, kh = sg % Hk;
+        if (L[m] == 0)
+            for (int i = threadIdx.x; i < G * D; i += kDecConsumerThreads)
+                out[(int64_t)m * H * D + (int64_t)(kh * G) * D + i] = 0.0f;
+    }
+
+    const int seg = lane % C::LPR;         // float4 column of this lane
+    const int rgrp = lane / C::LPR;        // row group within a pass
+    float* sc = sc_all + warp * C::ENTRIES;
+
+    float4 qv[G];
+    float acc[G][4];
+    float m_run = -INFINITY, l_run = 0.0f;
+    bool ok = true;
+    int it = 0;
+    int64_t pos = r0;
+    while (pos < r1) {
+        int m, kh;
+        int64_t seg_start;
+        locate(pos, P, L, Hk, m, kh, seg_start);
+        const int64_t seg_end = seg_start + L[m];
+        const int64_t piece_end = min(r1, seg_end);
+        // q of the G heads sharing kv head kh, pre-scaled so scores are in log2 units
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float4 t = __ldg(reinterpret_cast<const float4*>(q + (int64_t)m * H * D + (int64_t)(kh * G + h) * D) + seg);
+            qv[h] = make_float4(t.x * scale_log2, t.y * scale_log2, t.z * scale_log2, t.w * scale_log2);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[h][j] = 0.0f;
+        }
+        m_run = -INFINITY;
+        l_run = 0.0f;
+
+        for (int64_t t0 = pos; t0 < piece_end; t0 += kDecTileRows, ++it) {
+            const int s = it % C::NST;
+            const uint32_t ph = (uint32_t)(it / C::NST) & 1u;
+            if (ok) ok = mbar_wait(smem_addr(&bars[s]), ph, abort_flag, flags);
+            const int tile_rows = (int)min((int64_t)kDecTileRows, piece_end - t0);
+            const int nvalid = min(max(tile_rows - warp * kDecBatchRows, 0), kDecBatchRows);
+            if (ok && nvalid > 0) {
+                const float4* Ks = reinterpret_cast<const float4*>(smem + C::OFF_STAGES + (2 * s) * C::TILE_BYTES) +
+                                   (warp * kDecBatchRows) * C::LPR;
+                const float4* Vs = reinterpret_cast<const float4*>(smem + C::OFF_STAGES + (2 * s + 1) * C::TILE_BYTES) +
+                                   (warp * kDecBatchRows) * C::LPR;
+                // ---- partial dot products: pass p covers rows p*RPW .. p*RPW+RPW-1
+                float part[C::NV];
+#pragma unroll
+                for (int p = 0; p < C::PASSES; ++p) {
+                    const int row = p * C::RPW + rgrp;
+                    float4 kv = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (row < nvalid) kv = Ks[row * C::LPR + seg];
+#pragma unroll
+                    for (int h = 0; h < G; ++h)
+                        part[p * G + h] = qv[h].x * kv.x + qv[h].y * kv.y + qv[h].z * kv.z + qv[h].w * kv.w;
+                }
+                xpose_reduce<C::NV, C::LPR>(part, lane);
+                // ---- scatter the totals to sc[row * G + h]
+#pragma unroll
+                for (int t = 0; t < C::NVR; ++t) {
+                    int idx;
+                    bool writer;
+                    if (C::NV >= C::LPR) {
+                        idx = seg * (C::NV / C::LPR) + t;
+                        writer = true;
+                    } else {
+                        constexpr int dup = (C::NV >= C::LPR) ? 1 : C::LPR / C::NV;
+                        idx = seg / dup;
+                        writer = (seg % dup) == 0;
+                    }
+                    const int p = idx / G, h = idx % G;
+                    const int row = p * C::RPW + rgrp;
+                    if (writer) sc[row * G + h] = part[t];
+                }
+                __syncwarp();
+                // ---- online softmax over this batch (base 2)
+                float sv[C::EPL];
+                float bmax = -INFINITY;
+#pragma unroll
+                for (int k = 0; k < C::EPL; ++k) {
+                    const int e = lane + 32 * k;
+                    const bool valid = e < C::ENTRIES && (e / G) < nvalid;
+                    sv[k] = valid ? sc[e] : -INFINITY;
+                    bmax = fmaxf(bmax, sv[k]);
+                }
+#pragma unroll
+                for (int o = G; o < 32; o <<= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, o));
+                const float m_new = fmaxf(m_run, bmax);
+                const float alpha = (m_new == -INFINITY) ? 1.0f : fast_exp2(m_run - m_new);
+                float bsum = 0.0f;
+#pragma unroll
+                for (int k = 0; k < C::EPL; ++k) {
+                    const int e = lane + 32 * k;
+                    const float p = (sv[k] == -INFINITY) ? 0.0f : fast_exp2(sv[k] - m_new);
+                    bsum += p;
+                    if (e < C::ENTRIES) sc[e] = p;
+                }
+#pragma unroll
+                for (int o = G; o < 32; o <<= 1) bsum += __shfl_xor_sync(0xffffffffu, bsum, o);
+                l_run = l_run * alpha + bsum;
+                m_run = m_new;
+                __syncwarp();
+                // ---- rescale and accumulate P.V
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float a = __shfl_sync(0xffffffffu, alpha, h);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[h][j] *= a;
+                }
+#pragma unroll
+                for (int p = 0; p < C::PASSES; ++p) {
+                    const int row = p * C::RPW + rgrp;
+                    if (row < nvalid) {
+                        const float4 vv = Vs[row * C::LPR + seg];
+#pragma unroll
+                        for (int h = 0; h < G; ++h) {
+                            const float w = sc[row * G + h];
+                            acc[h][0] += w * vv.x;
+                            acc[h][1] += w * vv.y;
+                            acc[h][2] += w * vv.z;
+                            acc[h][3] += w * vv.w;
+                        }
+                    }
+                }
+            }
+            if (ok && *abort_flag) ok = false;
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(smem_addr(&bars[C::NST + s]));
+        }
+
+        // ---------------------------------------------------------- piece end
+        // rows of different row groups share the warp's running max: plain sums
+#pragma unroll
+        for (int o = C::LPR; o < 32; o <<= 1)
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[h][j] += __shfl_xor_sync(0xffffffffu, acc[h][j], o);
+        if (lane < C::LPR) {
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+                *reinterpret_cast<float4*>(red_acc + (warp * G + h) * D + seg * 4) =
+                    make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+        }
+        if (lane < G) {
+            red_ml[(warp * G + lane) * 2 + 0] = m_run;
+            red_ml[(warp * G + lane) * 2 + 1] = l_run;
+        }
+        named_barrier(1, kDecConsumerThreads);
+
+        const int sg = m * Hk + kh;
+        const int c_first = owner_of(seg_start, R, n);
+        const int c_last = owner_of(seg_end - 1, R, n);
+        const bool single = (c_first == c_last);
+        float* my_rec = records + (int64_t)(sg + c) * C::REC;
+        float* o_seg = out + (int64_t)m * H * D + (int64_t)(kh * G) * D;
+        for (int i = threadIdx.x; i < G * D; i += kDecConsumerThreads) {
+            const int h = i / D, d = i % D;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kDecConsumerWarps; ++w) mx = fmaxf(mx, red_ml[(w * G + h) * 2]);
+            float l = 0.0f, o = 0.0f;
+            if (mx != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < kDecConsumerWarps; ++w) {
+                    const float mw = red_ml[(w * G + h) * 2];
+                    const float f = (mw == -INFINITY) ? 0.0f : fast_exp2(mw - mx);
+                    l += red_ml[(w * G + h) * 2 + 1] * f;
+                    o += red_acc[(w * G + h) * D + d] * f;
+                }
+            }
+            if (single) {
+                o_seg[i] = l > 0.0f ? o / l : 0.0f;
+            } else {
+                my_rec[i] = o;
+                if (d == 0) {
+                    my_rec[G * D + h] = mx;
+                    my_rec[G * D + G + h] = l;
+                }
+            }
+        }
+        if (!single) {
+            __threadfence();
+            named_barrier(1, kDecConsumerThreads);
+            if (threadIdx.x == 0) {
+                // pieces = CTAs in [c_first, c_last] that own rows (a share is empty only when R < n)
+                int pieces = 0;
+                for (int cc = c_first; cc <= c_last; ++cc)
+                    pieces += share_begin(cc, R, n) < share_begin(cc + 1, R, n);
+                int last = 0;
+                if (ok) last = (atomicAdd(tickets + sg, 1) == pieces - 1);
+                *last_flag = last;
+            }
+            named_barrier(1, kDecConsumerThreads);
+            if (*last_flag) {
+                __threadfence();
+                for (int i = threadIdx.x; i < G * D; i += kDecConsumerThreads) {
+                    const int h = i / D;
+                    float mx = -INFINITY;
+                    for (int cc = c_first; cc <= c_last; ++cc)
+                        if (share_begin(cc, R, n) < share_begin(cc + 1, R, n))
+                            mx = fmaxf(mx, __ldcg(records + (int64_t)(sg + cc) * C::REC + G * D + h));
+                    float l = 0.0f, o = 0.0f;
+                    if (mx != -INFINITY) {
+                        for (int cc = c_first; cc <= c_last; ++cc) {
+                            if (share_begin(cc, R, n) >= share_begin(cc + 1, R, n)) continue;
+                            const float* rec = records + (int64_t)(sg + cc) * C::REC;
+                            const float mc = __ldcg(rec + G * D + h);
+                            const float f = (mc == -INFINITY) ? 0.0f : fast_exp2(mc - mx);
+                            l += __ldcg(rec + G * D + G + h) * f;
+                            o += __ldcg(rec + i) * f;
+                        }
+                    }
+                    o_seg[i] = l > 0.0f ? o / l : 0.0f;
+                }
+                if (threadIdx.x == 0) tickets[sg] = 0;
+            }
+        }
+        named_barrier(1, kDecConsumerThreads);   // red_* free for the next piece
+        pos = piece_end;
+    }
+}
+
+// ------------------------------------------------------------------ host side
+bool decode_group_supported(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+
+template <int D, int G>
+static constexpr int rec_floats() { return DecCfg<D, G>::REC; }
+
+static int rec_floats_rt(int D, int G) {
+    return ((G * D + 2 * G) + 3) / 4 * 4;
+}
+
+static size_t tickets_bytes(int M, int Hk) { return ((size_t)M * Hk * 4 + 255) / 256 * 256; }
+
+size_t decode_workspace_bytes(int M, int H, int Hk, int D) {
+    const int G = H / Hk;
+    return tickets_bytes(M, Hk) + (size_t)(M * Hk + kDecMaxCtas) * rec_floats_rt(D, G) * 4;
+}
+
+template <int D, int G>
+static rkv_status launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
+    using C = DecCfg<D, G>;
+    static_assert(rec_floats<D, G>() == ((G * D + 2 * G) + 3) / 4 * 4, "record layout");
+    auto kern = decode_splitkv_kernel<D, G>;
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+            return check_launch("attn_decode_batched: shared-memory attribute");
+        attr_done[dev] = true;
+    }
+    int n = sm_count();
+    if (n <= 0) return set_error(RKV_ERR_LAUNCH, "attn_decode_batched: cannot query the SM count");
+    if (n > kDecMaxCtas) n = kDecMaxCtas;
+    int* tickets = static_cast<int*>(a.workspace);
+    float* records = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + tickets_bytes(a.M, a.Hk));
+    kern<<<n, kDecThreads, C::SMEM, stream>>>(a.q, a.k_cache, a.v_cache, a.o, a.M, a.Hk, a.Lmax, a.seq_lens,
+                                               a.scale * kLog2e, tickets, records, a.flags);
+    return check_launch("attn_decode_batched");
+}
+
+rkv_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+    const int G = a.H / a.Hk;
+#define RKV_DEC_CASE(DD, GG) \
+    if (a.D == DD && G == GG) return launch_decode_t<DD, GG>(a, stream);
+    RKV_DEC_CASE(16, 1) RKV_DEC_CASE(16, 2) RKV_DEC_CASE(16, 4) RKV_DEC_CASE(16, 8)
+    RKV_DEC_CASE(32, 1) RKV_DEC_CASE(32, 2) RKV_DEC_CASE(32, 4) RKV_DEC_CASE(32, 8)
+    RKV_DEC_CASE(64, 1) RKV_DEC_CASE(64, 2) RKV_DEC_CASE(64, 4) RKV_DEC_CASE(64, 8)
+    RKV_DEC_CASE(128, 1) RKV_DEC_CASE(128, 2) RKV_DEC_CASE(128, 4) RKV_DEC_CASE(128, 8)
+#undef RKV_DEC_CASE
+    return set_error(RKV_ERR_UNSUPPORTED, "attn_decode_batched: head_dim %d with group %d", a.D, G);
+}
+
+}  // namespace rkv

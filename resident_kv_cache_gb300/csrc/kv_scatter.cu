@@ -1,0 +1,82 @@
+// kv_scatter.cu -- append new K/V rows into the resident batched cache.
+//
+//   cache[m, kh, start_pos[m] + t, :] = new[m, t, kh*D : (kh+1)*D]
+//
+// trueno-gpu 0.4.11, src/memory/resident/attention.rs, fn kv_cache_scatter_gpu
+// writes one interleaved [n_heads*head_dim] row into a head-first cache with one
+// block per head and one thread per element.  Here one launch covers every
+// sequence, token, kv head, and both K and V: grid.y = sequence, grid.x = chunks
+// of tokens, 16-byte vector loads/stores, and positions come from device memory
+// so the bounds check moves on chip (skipped tokens are counted).
+#include "rkv_internal.cuh"
+#include "rkv_launch.h"
+
+namespace rkv {
+
+constexpr int kScatterThreads = 256;
+constexpr int kScatterElemsPerBlock = 2048;   // float4 elements per tensor per block
+
+template <int D4>
+__global__ void __launch_bounds__(kScatterThreads)
+kv_scatter_kernel(const float4* __restrict__ k_new, const float4* __restrict__ v_new,
+                  float4* __restrict__ k_cache, float4* __restrict__ v_cache, int T, int Hk, int Lmax,
+                  int tokens_per_block, const int* __restrict__ start_pos, int* __restrict__ overflow,
+                  unsigned int* __restrict__ flags) {
+    const int m = blockIdx.y;
+    const int t0 = blockIdx.x * tokens_per_block;
+    const int n_tok = min(tokens_per_block, T - t0);
+    if (n_tok <= 0) return;
+    const int p0 = __ldg(start_pos + m);
+    const int row4 = Hk * D4;                         // float4 elements per token
+    const int total = n_tok * row4;
+    const int64_t src_base = ((int64_t)m * T + t0) * row4;
+    const int64_t seq_base = (int64_t)m * Hk * Lmax;  // first cache row of (m, kh = 0)
+
+    if (threadIdx.x < n_tok) {                        // per-token bounds accounting
+        const int64_t pos = (int64_t)p0 + t0 + threadIdx.x;
+        if (pos < 0 || pos >= Lmax) {
+            if (overflow) atomicAdd(overflow, 1);
+            if (p0 < 0) atomicOr(flags, RKV_FLAG_NEGATIVE_INPUT);
+        }
+    }
+
+#pragma unroll 4
+    for (int idx = threadIdx.x; idx < total; idx += kScatterThreads) {
+        const int j = idx / row4;                     // token within the block
+        const int rem = idx - j * row4;
+        const int kh = rem / D4;
+        const int d4 = rem - kh * D4;
+        const int64_t pos = (int64_t)p0 + t0 + j;
+        if (pos < 0 || pos >= Lmax) continue;
+        const float4 kv = __ldcs(k_new + src_base + idx);
+        const float4 vv = __ldcs(v_new + src_base + idx);
+        const int64_t dst = ((seq_base + (int64_t)kh * Lmax) + pos) * D4 + d4;
+        k_cache[dst] = kv;
+        v_cache[dst] = vv;
+    }
+}
+
+rkv_status launch_scatter(const float* k_new, const float* v_new, float* k_cache, float* v_cache, int M,
+                          int T, int Hk, int D, int Lmax, const int* start_pos, int* overflow,
+                          unsigned int* flags, cudaStream_t stream) {
+    const int row4 = Hk * (D / 4);
+    int tok = kScatterElemsPerBlock / row4;
+    if (tok < 1) tok = 1;
+    if (tok > kScatterThreads) tok = kScatterThreads;   // one accounting thread per token
+    const dim3 grid((unsigned)((T + tok - 1) / tok), (unsigned)M);
+    const dim3 block(kScatterThreads);
+    auto k4 = reinterpret_cast<const float4*>(k_new);
+    auto v4 = reinterpret_cast<const float4*>(v_new);
+    auto kc = reinterpret_cast<float4*>(k_cache);
+    auto vc = reinterpret_cast<float4*>(v_cache);
+    switch (D) {
+        case 16: kv_scatter_kernel<4><<<grid, block, 0, stream>>>(k4, v4, kc, vc, T, Hk, Lmax, tok, start_pos, overflow, flags); break;
+        case 32: kv_scatter_kernel<8><<<grid, block, 0, stream>>>(k4, v4, kc, vc, T, Hk, Lmax, tok, start_pos, overflow, flags); break;
+        case 64: kv_scatter_kernel<16><<<grid, block, 0, stream>>>(k4, v4, kc, vc, T, Hk, Lmax, tok, start_pos, overflow, flags); break;
+        case 128: kv_scatter_kernel<32><<<grid, block, 0, stream>>>(k4, v4, kc, vc, T, Hk, Lmax, tok, start_pos, overflow, flags); break;
+        default: return set_error(RKV_ERR_UNSUPPORTED, "kv_cache_scatter: head_dim %d", D);
+    }
+    return check_launch("kv_cache_scatter");
+}
+
+}  // namespace rkv

@@ -1,0 +1,48 @@
+// rkv_launch.h -- internal launcher interface between the C ABI and the kernels.
+#pragma once
+
+#include <cstddef>
+
+#include "../../include/rkv_attn.h"
+
+namespace rkv {
+
+// Batched decode handles at most 32 sequences (realizar
+// cache_from_cache_from_kv_cache.rs, fn init_batched_kv_cache_gpu).
+constexpr int kDecodeMaxSeqs = 32;
+
+struct PrefillArgs {
+    const float* q;
+    const float* k;
+    const float* v;
+    float* o;
+    int B, S, H, Hk, D;
+    bool causal;
+    const int* seq_lens;   // device, may be NULL
+    float scale;           // resolved (never 0)
+    unsigned int* flags;   // device flag word
+};
+
+struct DecodeArgs {
+    const float* q;
+    const float* k_cache;
+    const float* v_cache;
+    float* o;
+    int M, H, Hk, D, Lmax;
+    const int* seq_lens;
+    float scale;
+    void* workspace;
+    unsigned int* flags;
+};
+
+rkv_status launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
+bool decode_group_supported(int group);
+size_t decode_workspace_bytes(int M, int H, int Hk, int D);
+rkv_status launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+rkv_status launch_scatter(const float* k_new, const float* v_new, float* k_cache, float* v_cache, int M,
+                          int T, int Hk, int D, int Lmax, const int* start_pos, int* overflow,
+                          unsigned int* flags, cudaStream_t stream);
+
+}  // namespace rkv
