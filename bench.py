@@ -1,0 +1,439 @@
+#!/usr/bin/env python3
+"""Benchmark of the resident-attention hot path on GB300.
+
+One step is one pass over every operation of the path:
+  1. causal GQA prefill   B=4, S=2048, H=32, Hk=8, D=128   (attn_prefill)
+  2. cache fill           its K/V scattered into a [4,8,4096,128] cache (kv_cache_scatter)
+  3. batched decode step  M=32, H=32, Hk=8, D=128, cache [32,8,4096,128], lengths U{1..4096}:
+                          the new K/V row scattered at len-1 (kv_cache_scatter), then
+                          attn_decode_batched over len rows.
+The headline value is the decode step's KV-read bandwidth (GB/s of K and V rows
+read); the prefill's TFLOP/s (causal-counted) is reported beside it.  Inputs are
+seeded synthetic N(0,1) f32 and resident in HBM before timing; the per-step
+working set (1.07 GB of cache plus 201 MB of prefill inputs) is larger than L2.
+
+python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+Under torchrun each rank runs the same workload on its own GPU (weak scaling, no
+data-path collective); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from resident_kv_cache_gb300 import inputs  # noqa: E402
+
+METRIC = "decode KV-read GB/s & prefill attention TFLOP/s, % of GB300 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TF32_PER_BF16 = 1.1 / 2.25      # nominal dense TF32 : BF16 ratio
+PREFILL = inputs.CAUSAL_GQA
+DECODE = inputs.BATCHED_DECODE
+FILL_LEN = inputs.CAUSAL_GQA_CACHE_LEN
+WORKLOAD = ("causal GQA prefill B=4 S=2048 H=32 Hk=8 D=128 + cache fill into [4,8,4096,128] + "
+            "batched decode step M=32 H=32 Hk=8 D=128 Lmax=4096 lengths U{1..4096}")
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["rkv", "reference"], default="rkv")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.path = index, None, None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.1)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
+
+
+def kernel_hash(*files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "resident_kv_cache_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_FILES = {"prefill": ("prefill_simt.cu",), "decode": ("decode_splitkv.cu",), "scatter": ("kv_scatter.cu",)}
+
+
+def ncu_traffic(kernel):
+    """Per-launch DRAM bytes from the committed ncu summary, if taken on the current source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f).get(kernel)
+    if not d or d.get("source_hash") != kernel_hash(*KERNEL_FILES[kernel]):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------- workload
+def decode_bytes(lens):
+    M, H, Hk, D = DECODE.M, DECODE.H, DECODE.Hk, DECODE.D
+    kv = 2.0 * Hk * D * 4 * float(np.sum(lens))
+    return kv, kv + 2.0 * M * H * D * 4      # K/V rows read; plus q read and o written
+
+
+def scatter_bytes(M, T, Hk, D):
+    return 2.0 * 2.0 * M * T * Hk * D * 4    # K and V, read + write
+
+
+class Workload:
+    def __init__(self, torch, rkv, dev):
+        self.torch, self.rkv, self.dev = torch, rkv, dev
+        P, Dd = PREFILL, DECODE
+        q, k, v = inputs.prefill_inputs(P)
+        self.host_prefill = (q, k, v)
+        self.q, self.k, self.v = (torch.from_numpy(a).to(dev) for a in (q, k, v))
+        self.o = torch.empty((P.B, P.S, P.H * P.D), device=dev)
+        self.kc3 = torch.zeros((P.B, P.Hk, FILL_LEN, P.D), device=dev)
+        self.vc3 = torch.zeros((P.B, P.Hk, FILL_LEN, P.D), device=dev)
+        self.start3 = torch.zeros(P.B, dtype=torch.int32, device=dev)
+        x = inputs.batched_decode_inputs(Dd)
+        self.host_decode = x
+        self.kc = torch.from_numpy(x["k_cache"]).to(dev)
+        self.vc = torch.from_numpy(x["v_cache"]).to(dev)
+        self.qd = torch.from_numpy(x["q"]).to(dev)
+        self.kn = torch.from_numpy(x["k_new"]).to(dev)
+        self.vn = torch.from_numpy(x["v_new"]).to(dev)
+        self.sp = torch.from_numpy(x["start_pos"]).to(dev)
+        self.ln = torch.from_numpy(x["lens"]).to(dev)
+        self.od = torch.empty((Dd.M, Dd.H * Dd.D), device=dev)
+        self.nws = rkv.attn_decode_workspace_bytes(Dd.M, Dd.H, Dd.Hk, Dd.D, Dd.Lmax)
+        self.ws = torch.zeros(self.nws, dtype=torch.uint8, device=dev)
+        self.lens = x["lens"]
+
+    def prefill_part(self):
+        P, r = PREFILL, self.rkv
+        r.attn_prefill(self.q, self.k, self.v, self.o, P.B, P.S, P.H, P.Hk, P.D, True)
+
+    def fill_part(self):
+        P = PREFILL
+        self.rkv.kv_cache_scatter(self.k, self.v, self.kc3, self.vc3, P.B, P.S, P.Hk, P.D, FILL_LEN, self.start3)
+
+    def decode_scatter_part(self):
+        Dd = DECODE
+        self.rkv.kv_cache_scatter(self.kn, self.vn, self.kc, self.vc, Dd.M, 1, Dd.Hk, Dd.D, Dd.Lmax, self.sp)
+
+    def decode_part(self):
+        Dd = DECODE
+        self.rkv.attn_decode_batched(self.qd, self.kc, self.vc, self.od, Dd.M, Dd.H, Dd.Hk, Dd.D, Dd.Lmax,
+                                     self.ln, 0.0, self.ws, self.nws)
+
+
+LAUNCHES_PER_STEP = 4   # prefill, cache-fill scatter, decode-step scatter, decode
+
+
+def run_rkv(args, rank, world, torch, dist):
+    from resident_kv_cache_gb300 import binding as rkv
+    from resident_kv_cache_gb300 import build as rkv_build
+    if rank == 0 or not os.path.exists(rkv_build.LIB):
+        rkv_build.build()
+    if dist is not None:
+        dist.barrier()
+    rkv.load()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    W = Workload(torch, rkv, dev)
+    parts = [W.prefill_part, W.fill_part, W.decode_scatter_part, W.decode_part]
+
+    def step(evs=None):
+        for i, fn in enumerate(parts):
+            if evs is not None:
+                evs[i].record(stream)
+            fn()
+        if evs is not None:
+            evs[len(parts)].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    K = args.steps
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)] for _ in range(K)]
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(K):
+        step(events[s])
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    total_ms = t_start.elapsed_time(t_stop)
+    part_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(len(parts))] for e in events]).mean(axis=0)
+    flags = rkv.rkv_read_device_flags()
+    if flags & rkv.RKV_FLAG_WAIT_TIMEOUT:
+        raise RuntimeError("device reported a wait timeout during the benchmark")
+
+    # max over ranks
+    vals = torch.tensor([total_ms, *part_ms.tolist()], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    total_ms, part_ms = float(vals[0]), vals[1:].cpu().numpy()
+    ms_step = total_ms / K
+    prefill_ms, fill_ms, dsc_ms, dec_ms = (float(x) for x in part_ms)
+
+    kv_bytes, dec_all_bytes = decode_bytes(W.lens)
+    decode_step_gbs = kv_bytes / ((dsc_ms + dec_ms) * 1e-3) / 1e9
+    value = decode_step_gbs * world
+    prefill_tflops = PREFILL.flops / (prefill_ms * 1e-3) / 1e12
+    peaks, peak_kind = load_peaks()
+    hbm = peaks["hbm_gbs"]
+    tf32 = peaks["bf16_tflops"] * TF32_PER_BF16
+    fill_b = scatter_bytes(PREFILL.B, PREFILL.S, PREFILL.Hk, PREFILL.D)
+    rooflines = {
+        "prefill": {"bound": "tensor", "achieved": prefill_tflops, "peak": tf32, "unit": "TFLOP/s",
+                    "frac": prefill_tflops / tf32, "traffic": ncu_traffic("prefill"),
+                    "peak_note": f"{peak_kind} bf16 burst x nominal TF32/BF16 ratio 1.1/2.25",
+                    "ms": prefill_ms},
+        "decode": {"bound": "hbm", "achieved": dec_all_bytes / (dec_ms * 1e-3) / 1e9, "peak": hbm,
+                   "unit": "GB/s", "frac": dec_all_bytes / (dec_ms * 1e-3) / 1e9 / hbm,
+                   "traffic": ncu_traffic("decode"), "peak_note": f"{peak_kind} copy bandwidth",
+                   "ms": dec_ms},
+        "scatter_fill": {"bound": "hbm", "achieved": fill_b / (fill_ms * 1e-3) / 1e9, "peak": hbm,
+                         "unit": "GB/s", "frac": fill_b / (fill_ms * 1e-3) / 1e9 / hbm,
+                         "traffic": ncu_traffic("scatter"), "peak_note": f"{peak_kind} copy bandwidth",
+                         "ms": fill_ms},
+    }
+    dominant = max(rooflines, key=lambda k: rooflines[k]["ms"])
+    out = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 (prefill products on TF32 tensor cores)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 (1.07 GB decode cache + 201 MB prefill "
+                   "inputs per step)", "seeds": [inputs.SEED_Q, inputs.SEED_K, inputs.SEED_V, inputs.SEED_LEN],
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "values": {"decode_step_kv_read_gbs": decode_step_gbs, "decode_kernel_gbs":
+                   rooflines["decode"]["achieved"], "prefill_tflops": prefill_tflops,
+                   "cache_fill_gbs": rooflines["scatter_fill"]["achieved"]},
+        "parts_ms": {"prefill": prefill_ms, "cache_fill_scatter": fill_ms, "decode_scatter": dsc_ms,
+                     "decode": dec_ms},
+        "roofline": dict(rooflines[dominant], kernel=dominant),
+        "rooflines": rooflines,
+        "gpu_launches": LAUNCHES_PER_STEP * K,
+        "clocks": clocks,
+    }
+    if not args.no_e2e:
+        out["e2e"] = run_e2e(W, torch, rkv, stream, K=max(3, min(K, 10)))
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        out["cpu_baseline"] = cpu_baseline(W.host_decode, W.host_prefill)
+    return out
+
+
+def run_e2e(W, torch, rkv, stream, K):
+    """Same step through the public API with inputs in pinned host memory: every step copies
+    its inputs host->device and its outputs device->host inside the timed region."""
+    P, Dd = PREFILL, DECODE
+    hq, hk, hv = (torch.from_numpy(a).pin_memory() for a in W.host_prefill)
+    x = W.host_decode
+    hqd, hkn, hvn = (torch.from_numpy(x[n]).pin_memory() for n in ("q", "k_new", "v_new"))
+    hsp, hln = torch.from_numpy(x["start_pos"]).pin_memory(), torch.from_numpy(x["lens"]).pin_memory()
+    ho = torch.empty(W.o.shape, dtype=torch.float32).pin_memory()
+    hod = torch.empty(W.od.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hqd, hkn, hvn, hsp, hln))
+    d2h = ho.numel() * 4 + hod.numel() * 4
+
+    def step(evs):
+        evs[0].record(stream)
+        W.q.copy_(hq, non_blocking=True); W.k.copy_(hk, non_blocking=True); W.v.copy_(hv, non_blocking=True)
+        W.prefill_part()
+        W.fill_part()
+        ho.copy_(W.o, non_blocking=True)
+        evs[1].record(stream)
+        W.qd.copy_(hqd, non_blocking=True); W.kn.copy_(hkn, non_blocking=True); W.vn.copy_(hvn, non_blocking=True)
+        W.sp.copy_(hsp, non_blocking=True); W.ln.copy_(hln, non_blocking=True)
+        W.decode_scatter_part()
+        W.decode_part()
+        hod.copy_(W.od, non_blocking=True)
+        evs[2].record(stream)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K + 2)]
+    for i in range(2):
+        step(evs[i])
+    torch.cuda.synchronize()
+    for i in range(2, K + 2):
+        step(evs[i])
+    torch.cuda.synchronize()
+    pre = np.mean([e[0].elapsed_time(e[1]) for e in evs[2:]])
+    dec = np.mean([e[1].elapsed_time(e[2]) for e in evs[2:]])
+    kv_bytes, _ = decode_bytes(W.lens)
+    return {"value": kv_bytes / (dec * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "prefill_tflops": PREFILL.flops / (pre * 1e-3) / 1e12,
+            "ms_per_step": float(pre + dec), "steps": K,
+            "note": "decode KV cache stays resident; per-step inputs and outputs cross PCIe/C2C"}
+
+
+def cpu_baseline(host_decode, host_prefill, budget_s=20.0):
+    """The oracle (test infrastructure) timed on this host's cores on a bounded sample."""
+    import oracle
+    oracle.build()
+    x = host_decode
+    Dd, P = DECODE, PREFILL
+    # decode: whole batched decode step (all 32 sequences)
+    hk, hv = x["k_cache"].copy(), x["v_cache"].copy()
+    t0 = time.perf_counter()
+    oracle.scatter(x["k_new"], x["v_new"], hk, hv, Dd.M, 1, Dd.Hk, Dd.D, Dd.Lmax, x["start_pos"],
+                   inplace=True)
+    t1 = time.perf_counter()
+    oracle.decode(x["q"], hk, hv, Dd.M, Dd.H, Dd.Hk, Dd.D, Dd.Lmax, x["lens"])
+    t2 = time.perf_counter()
+    kv_bytes, _ = decode_bytes(x["lens"])
+    dec_gbs = kv_bytes / (t2 - t1) / 1e9
+    # prefill: a sample of query rows, scaled by the FLOPs those rows carry
+    q, k, v = host_prefill
+    n_rows = 512
+    rows = inputs.sample_indices(P.B * P.H * P.S, n_rows, 5)
+    t3 = time.perf_counter()
+    oracle.prefill_rows(q, k, v, P.B, P.S, P.H, P.Hk, P.D, True, rows)
+    t4 = time.perf_counter()
+    flops = float(np.sum(4.0 * P.D * ((rows % P.S) + 1)))
+    return {"value": dec_gbs, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "one whole batched decode step (32 sequences) for GB/s; 512 random causal prefill "
+                      "rows for TFLOP/s", "prefill_tflops": flops / (t4 - t3) / 1e12,
+            "seconds": round(t4 - t0, 2), "scatter_s": round(t1 - t0, 3)}
+
+
+def run_reference(args):
+    """Reference arm: the oracle, as it stands, on the host cores, same metric and unit."""
+    import oracle
+    oracle.build()
+    x = inputs.batched_decode_inputs(DECODE)
+    Dd, P = DECODE, PREFILL
+    q, k, v = inputs.prefill_inputs(P)
+    kv_bytes, _ = decode_bytes(x["lens"])
+    rows = inputs.sample_indices(P.B * P.H * P.S, 64, 9)
+    flops = float(np.sum(4.0 * P.D * ((rows % P.S) + 1)))
+
+    hk, hv = x["k_cache"], x["v_cache"]      # the reference arm owns these arrays
+
+    def step():
+        a = time.perf_counter()
+        oracle.scatter(x["k_new"], x["v_new"], hk, hv, Dd.M, 1, Dd.Hk, Dd.D, Dd.Lmax, x["start_pos"],
+                       inplace=True)
+        b = time.perf_counter()
+        oracle.decode(x["q"], hk, hv, Dd.M, Dd.H, Dd.Hk, Dd.D, Dd.Lmax, x["lens"])
+        c = time.perf_counter()
+        oracle.prefill_rows(q, k, v, P.B, P.S, P.H, P.Hk, P.D, True, rows)
+        d = time.perf_counter()
+        return b - a, c - b, d - c
+
+    for _ in range(max(0, args.warmup)):
+        step()
+    res = [step() for _ in range(args.steps)]
+    dec = np.mean([r[0] + r[1] for r in res])
+    pre = np.mean([r[2] for r in res])
+    value = kv_bytes / dec / 1e9
+    cores = oracle.num_threads()
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(np.mean([sum(r) for r in res]) * 1e3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": "decode: whole batched decode step; prefill: 64 causal rows"},
+            "values": {"decode_step_kv_read_gbs": value, "prefill_tflops": flops / pre / 1e12},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": "whole batched decode step (scatter + decode of 32 sequences) per step"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    out = run_rkv(args, rank, world, torch, dist)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

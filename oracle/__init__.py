@@ -158,11 +158,18 @@ def decode(q, k_cache, v_cache, M, H, Hk, D, Lmax, seq_lens, scale=None):
     return o
 
 
-def scatter(k_new, v_new, k_cache, v_cache, M, T, Hk, D, Lmax, start_pos):
-    """In-place scatter into (copies of) the caches; returns (k_cache, v_cache, overflow)."""
+def scatter(k_new, v_new, k_cache, v_cache, M, T, Hk, D, Lmax, start_pos, inplace=False):
+    """Scatter into copies of the caches (or into the given arrays themselves when inplace,
+    which must then be C-contiguous float32); returns (k_cache, v_cache, overflow)."""
     kn, vn = _f32(k_new), _f32(v_new)
-    kc = np.array(k_cache, dtype=np.float32, copy=True, order="C")
-    vc = np.array(v_cache, dtype=np.float32, copy=True, order="C")
+    if inplace:
+        kc, vc = k_cache, v_cache
+        for a in (kc, vc):
+            if a.dtype != np.float32 or not a.flags.c_contiguous:
+                raise ValueError("in-place scatter needs C-contiguous float32 caches")
+    else:
+        kc = np.array(k_cache, dtype=np.float32, copy=True, order="C")
+        vc = np.array(v_cache, dtype=np.float32, copy=True, order="C")
     sp = _i32(start_pos)
     ov = np.zeros(1, dtype=np.int32)
     rc = _load().rkv_oracle_scatter(_ptr(kn), _ptr(vn), _ptr(kc), _ptr(vc), M, T, Hk, D, Lmax,

@@ -25,3 +25,12 @@ def cuda_available() -> bool:
         return torch.cuda.is_available()
     except Exception:
         return False
+
+
+@pytest.fixture(scope="session")
+def rkv():
+    """The built CUDA library's binding (builds in-tree if needed)."""
+    from resident_kv_cache_gb300 import binding, build
+    build.build()
+    binding.load()
+    return binding

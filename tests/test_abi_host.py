@@ -1,0 +1,125 @@
+"""Host-only checks of the C ABI (no GPU needed).
+
+The library builds for sm_103a, loads, exports every function the header
+declares, and rejects invalid arguments on the host before touching the GPU --
+the pages' hardware-free validation tests (trustformers-core attention.rs,
+mod plan_tests: exact fit, empty, overrun) carried over to this ABI.
+"""
+import ctypes
+
+import pytest
+
+from resident_kv_cache_gb300 import binding, build
+
+pytestmark = pytest.mark.filterwarnings("ignore")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def test_library_exports_every_declared_function(lib):
+    names = binding.declared_functions()
+    assert set(names) >= {"attn_prefill", "attn_decode_batched", "attn_decode_workspace_bytes",
+                          "kv_cache_scatter", "rkv_last_error", "rkv_status_string",
+                          "rkv_read_device_flags", "rkv_version"}
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/rkv_attn.h but not exported"
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert binding.rkv_status_string(s)
+    assert binding.rkv_version() >= 1
+
+
+def _expect(status, fn, *args, **kw):
+    with pytest.raises(binding.RkvError) as e:
+        fn(*args, **kw)
+    assert e.value.status == status, str(e.value)
+    assert e.value.message
+    return e.value
+
+
+A = 1 << 20   # a fake 16-byte-aligned address: never dereferenced, validation fails first
+INV, UNS = binding.RKV_ERR_INVALID_ARG, binding.RKV_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("args,status", [
+    ((A, A, A, A, 1, 8, 3, 2, 64, 1), INV),      # n_heads % n_kv_heads != 0
+    ((A, A, A, A, 1, 8, 4, 2, 48, 1), UNS),      # head_dim not supported
+    ((A, A, A, A, 1, 8, 4, 0, 64, 1), INV),      # n_kv_heads == 0
+    ((A, A, A, A, -1, 8, 4, 2, 64, 1), INV),     # negative batch
+    ((A, A, A, A, 1, -8, 4, 2, 64, 1), INV),     # negative seq_len
+    ((None, A, A, A, 1, 8, 4, 2, 64, 1), INV),   # NULL q
+    ((A + 4, A, A, A, 1, 8, 4, 2, 64, 1), INV),  # misaligned q
+    ((A, A, A, A, 1, 8, 4, 2, 64, 1), INV),      # o aliases q
+    ((A, A, A, 2 * A, 1 << 16, 8, 4, 2, 64, 1), UNS),  # batch*heads beyond grid limit
+])
+def test_prefill_host_validation(lib, args, status):
+    _expect(status, binding.attn_prefill, *args, stream=0)
+
+
+def test_prefill_rejects_bad_scale(lib):
+    _expect(INV, binding.attn_prefill, A, A, A, 2 * A, 1, 8, 4, 2, 64, 1, scale=-1.0, stream=0)
+    _expect(INV, binding.attn_prefill, A, A, A, 2 * A, 1, 8, 4, 2, 64, 1, scale=float("nan"), stream=0)
+
+
+def test_zero_sized_work_is_a_noop(lib):
+    binding.attn_prefill(None, None, None, None, 0, 8, 4, 2, 64, 1, stream=0)
+    binding.attn_prefill(None, None, None, None, 2, 0, 4, 2, 64, 0, stream=0)
+    binding.kv_cache_scatter(None, None, None, None, 0, 1, 8, 128, 16, None, stream=0)
+    binding.kv_cache_scatter(None, None, None, None, 4, 0, 8, 128, 16, None, stream=0)
+    binding.attn_decode_batched(None, None, None, None, 0, 32, 8, 128, 16, None, 0.0, None, 0,
+                                stream=0)
+
+
+@pytest.mark.parametrize("args,status", [
+    ((A, A, A, A, 33, 32, 8, 128, 4096, A, 0.0, A, 1 << 30), INV),   # M > 32 (batched cache limit)
+    ((A, A, A, A, 4, 32, 8, 96, 4096, A, 0.0, A, 1 << 30), UNS),     # head_dim
+    ((A, A, A, A, 4, 48, 3, 128, 4096, A, 0.0, A, 1 << 30), UNS),    # group 16 unsupported
+    ((A, A, A, A, 4, 32, 8, 128, 0, A, 0.0, A, 1 << 30), INV),       # max_len 0
+    ((A, A, A, A, 4, 32, 8, 128, 4096, None, 0.0, A, 1 << 30), INV), # seq_lens NULL
+    ((A, A, A, A, 4, 32, 8, 128, 4096, A, 0.0, A + 16, 1 << 30), INV),  # workspace alignment
+    ((A, A, A, A, 4, 32, 8, 128, 4096, A, 0.0, A, 64), INV),         # workspace too small
+])
+def test_decode_host_validation(lib, args, status):
+    _expect(status, binding.attn_decode_batched, *args, stream=0)
+
+
+def test_decode_workspace_query(lib):
+    n = binding.attn_decode_workspace_bytes(32, 32, 8, 128, 4096)
+    assert n > 0 and n % 4 == 0
+    assert binding.attn_decode_workspace_bytes(33, 32, 8, 128, 4096) == 0
+    assert binding.attn_decode_workspace_bytes(4, 32, 7, 128, 4096) == 0
+    # grows with the record size
+    assert binding.attn_decode_workspace_bytes(4, 32, 8, 64, 4096) < \
+        binding.attn_decode_workspace_bytes(4, 32, 8, 128, 4096)
+
+
+@pytest.mark.parametrize("args,status", [
+    ((A, A, A, A, 33, 1, 8, 128, 4096, A), INV),    # M > 32
+    ((A, A, A, A, 4, 5000, 8, 128, 4096, A), INV),  # T > max_len
+    ((A, A, A, A, 4, 1, 8, 80, 4096, A), UNS),      # head_dim
+    ((A, A, A, A, 4, 1, 8, 128, 4096, None), INV),  # start_pos NULL
+    ((A, A + 8, A, A, 4, 1, 8, 128, 4096, A), INV),  # misaligned v_new
+    ((A, A, A, A, 4, -1, 8, 128, 4096, A), INV),    # negative T
+])
+def test_scatter_host_validation(lib, args, status):
+    _expect(status, binding.kv_cache_scatter, *args, stream=0)
+
+
+def test_last_error_is_per_call(lib):
+    _expect(INV, binding.attn_prefill, A, A, A, A, 1, 8, 3, 2, 64, 1, stream=0)
+    assert "multiple" in binding.rkv_last_error()
+    binding.attn_prefill(None, None, None, None, 0, 8, 4, 2, 64, 1, stream=0)
+    assert binding.rkv_last_error() == ""
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(FileNotFoundError):
+        binding.load()

@@ -1,0 +1,137 @@
+"""Prefill attention on the GPU against the oracle.
+
+Tolerance: 3e-3 max abs and 1e-3 mean abs on N(0,1) inputs (TF32 tensor-core
+products with f32 accumulation).  Semantics: trueno-gpu attention.rs,
+fn batched_multihead_attention_optimized (interleaved layout, non-causal) and
+trustformers-core attention.rs, fn attention_prefill_gpu_to_gpu (causal).
+"""
+import numpy as np
+import pytest
+
+from resident_kv_cache_gb300 import inputs
+from tests.gpu_util import Guarded, assert_close, empty_guarded, torch_cuda
+
+pytestmark = pytest.mark.gpu
+MAX_ABS, MEAN_ABS = 3e-3, 1e-3
+
+
+def _prefill(rkv, torch, q, k, v, B, S, H, Hk, D, causal, seq_lens=None, scale=0.0):
+    g_q, g_k, g_v = Guarded(torch, q), Guarded(torch, k), Guarded(torch, v)
+    g_o = empty_guarded(torch, (B, S, H * D))
+    g_l = None if seq_lens is None else Guarded(torch, np.asarray(seq_lens, np.int32), np.int32)
+    rkv.attn_prefill(g_q.t, g_k.t, g_v.t, g_o.t, B, S, H, Hk, D, causal,
+                     None if g_l is None else g_l.t, scale)
+    torch.cuda.synchronize()
+    for g in (g_q, g_k, g_v, g_o):
+        assert g.guards_intact()
+    return g_o.numpy()
+
+
+CASES = [
+    # B, S, H, Hk, D, causal, seq_lens
+    (1, 1, 1, 1, 16, False, None),
+    (1, 7, 2, 1, 32, True, None),
+    (2, 130, 4, 2, 64, True, None),
+    (2, 130, 4, 2, 64, False, None),
+    (1, 300, 8, 2, 128, True, None),
+    (1, 300, 8, 8, 128, False, None),
+    (3, 257, 4, 4, 16, True, [257, 129, 1]),
+    (2, 200, 6, 3, 32, False, [200, 77]),
+    (2, 384, 4, 1, 128, True, [384, 250]),
+    (1, 129, 2, 2, 64, False, [0]),
+]
+
+
+@pytest.mark.parametrize("ci", range(len(CASES)))
+def test_prefill_matches_oracle(rkv, oracle_mod, ci):
+    torch = torch_cuda()
+    B, S, H, Hk, D, causal, lens = CASES[ci]
+    q = inputs.normal((B, S, H * D), (ci, 10))
+    k = inputs.normal((B, S, Hk * D), (ci, 11))
+    v = inputs.normal((B, S, Hk * D), (ci, 12))
+    got = _prefill(rkv, torch, q, k, v, B, S, H, Hk, D, causal, lens)
+    want = oracle_mod.prefill(q, k, v, B, S, H, Hk, D, causal, seq_lens=lens)
+    assert_close(got, want, MAX_ABS, MEAN_ABS, what=f"case {ci}")
+    if lens is not None:          # padded query rows are exactly zero
+        for b, n in enumerate(lens):
+            assert np.all(got[b, n:] == 0.0)
+
+
+def test_prefill_explicit_scale(rkv, oracle_mod):
+    torch = torch_cuda()
+    B, S, H, Hk, D = 1, 150, 4, 2, 64
+    q, k, v = (inputs.normal((B, S, n * D), (33, t)) for t, n in enumerate((H, Hk, Hk)))
+    got = _prefill(rkv, torch, q, k, v, B, S, H, Hk, D, True, scale=0.05)
+    want = oracle_mod.prefill(q, k, v, B, S, H, Hk, D, True, scale=0.05)
+    assert_close(got, want, MAX_ABS, MEAN_ABS)
+
+
+def test_tiny_mha_prefill_full(rkv, oracle_mod):
+    """seq_len=32, n_heads=n_kv_heads=2, head_dim=16, non-causal, scale 1/4."""
+    torch = torch_cuda()
+    s = inputs.TINY
+    q, k, v = inputs.prefill_inputs(s)
+    got = _prefill(rkv, torch, q, k, v, s.B, s.S, s.H, s.Hk, s.D, s.causal)
+    want = oracle_mod.prefill(q, k, v, s.B, s.S, s.H, s.Hk, s.D, s.causal)
+    assert_close(got, want, MAX_ABS, MEAN_ABS, what="tiny")
+
+
+def test_encoder_prefill_full(rkv, oracle_mod):
+    """seq_len=1500, 8 heads of 64 in a [1500,512] activation, non-causal (whole output)."""
+    torch = torch_cuda()
+    s = inputs.ENCODER
+    q, k, v = inputs.prefill_inputs(s)
+    got = _prefill(rkv, torch, q, k, v, s.B, s.S, s.H, s.Hk, s.D, s.causal)
+    want = oracle_mod.prefill(q, k, v, s.B, s.S, s.H, s.Hk, s.D, s.causal)
+    assert_close(got, want, MAX_ABS, MEAN_ABS, what="encoder")
+
+
+def _causal_gqa_rows(s, n_random=400):
+    rows = set()
+    for b in range(s.B):
+        for h in (0, 1, 5, s.H - 1):
+            for i in (0, 1, 2, 127, 128, 129, 1023, 1024, s.S - 2, s.S - 1):
+                rows.add((b * s.H + h) * s.S + i)
+    rows.update(int(r) for r in inputs.sample_indices(s.B * s.H * s.S, n_random, 17))
+    return np.array(sorted(rows), np.int64)
+
+
+def test_causal_gqa_prefill_full_size_sampled(rkv, oracle_mod):
+    """B=4, S=2048, H=32, Hk=8, D=128, causal: the whole output is computed on the GPU and
+    a sample of rows (tile edges, first/last rows, every 4th head group) checked."""
+    torch = torch_cuda()
+    s = inputs.CAUSAL_GQA
+    q, k, v = inputs.prefill_inputs(s)
+    dq, dk, dv = (torch.from_numpy(a).cuda() for a in (q, k, v))
+    o = torch.full((s.B, s.S, s.H * s.D), float("nan"), device="cuda")
+    rkv.attn_prefill(dq, dk, dv, o, s.B, s.S, s.H, s.Hk, s.D, True)
+    torch.cuda.synchronize()
+    got_all = o.cpu().numpy()
+    assert np.all(np.isfinite(got_all))
+    rows = _causal_gqa_rows(s)
+    want = oracle_mod.prefill_rows(q, k, v, s.B, s.S, s.H, s.Hk, s.D, True, rows)
+    b, h, i = rows // (s.H * s.S), (rows // s.S) % s.H, rows % s.S
+    got = np.stack([got_all[bb, ii, hh * s.D:(hh + 1) * s.D] for bb, hh, ii in zip(b, h, i)])
+    assert_close(got, want, MAX_ABS, MEAN_ABS, what="causal GQA sample")
+
+
+def test_gpu_decode_equals_last_causal_prefill_row(rkv):
+    """The pages' invariant (trustformers-core attention.rs, mod gpu_tests, decode test),
+    checked between this library's own two kernels."""
+    torch = torch_cuda()
+    S, H, Hk, D, L = 333, 16, 4, 128, 512
+    q, k, v = (inputs.normal((1, S, n * D), (44, t)) for t, n in enumerate((H, Hk, Hk)))
+    dq, dk, dv = (torch.from_numpy(a).cuda() for a in (q, k, v))
+    o = torch.empty((1, S, H * D), device="cuda")
+    rkv.attn_prefill(dq, dk, dv, o, 1, S, H, Hk, D, True)
+    kc = torch.zeros((1, Hk, L, D), device="cuda")
+    vc = torch.zeros((1, Hk, L, D), device="cuda")
+    start = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rkv.kv_cache_scatter(dk, dv, kc, vc, 1, S, Hk, D, L, start)
+    n = rkv.attn_decode_workspace_bytes(1, H, Hk, D, L)
+    ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    lens = torch.full((1,), S, dtype=torch.int32, device="cuda")
+    od = torch.empty((1, H * D), device="cuda")
+    rkv.attn_decode_batched(dq[:, S - 1, :].contiguous(), kc, vc, od, 1, H, Hk, D, L, lens, 0.0, ws, n)
+    torch.cuda.synchronize()
+    assert_close(od.cpu().numpy(), o[:, S - 1, :].cpu().numpy(), MAX_ABS)
