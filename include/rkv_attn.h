@@ -139,6 +139,29 @@ rkv_status attn_decode_batched(const float* q, const float* k_cache, const float
                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * attn_decode_batched without a caller workspace, for callers that cannot
+ * allocate device memory when they decode (an allocator owned by someone
+ * else, a plugin host that forbids allocation after start-up, a real-time
+ * loop that must not block in cudaMalloc).  The reference pages have no
+ * counterpart: their decode paths allocate per call.
+ *
+ * Same arguments, semantics and results as attn_decode_batched, minus the
+ * workspace.  The scratch is a fixed 4 MiB array in the library's own device
+ * memory, held on every GPU that loads the library until the process exits;
+ * sizes whose workspace (attn_decode_workspace_bytes) exceeds it are rejected
+ * with RKV_ERR_UNSUPPORTED.  Nothing is allocated: no cudaMalloc, no library
+ * allocator.  The first call on a device looks up the array's device address
+ * (make it before any stream capture).  Each call clears the part of the
+ * array that must start at zero with an asynchronous memset on `stream`.
+ * All calls share the one array: calls that overlap on the GPU (different
+ * streams or host threads on one device) race and give wrong results.
+ */
+rkv_status attn_decode_batched_noalloc(const float* q, const float* k_cache,
+                                       const float* v_cache, float* o, int M, int n_heads,
+                                       int n_kv_heads, int head_dim, int max_len,
+                                       const int* seq_lens, float scale, cudaStream_t stream);
+
+/*
  * Appends T new K/V rows per sequence into the resident cache.
  *
  * Cites: trueno-gpu attention.rs, fn kv_cache_scatter_gpu (interleaved

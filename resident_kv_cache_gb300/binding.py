@@ -69,6 +69,8 @@ def load():
     lib.attn_decode_workspace_bytes.argtypes = [I, I, I, I, I]
     lib.attn_decode_batched.restype = I
     lib.attn_decode_batched.argtypes = [P, P, P, P, I, I, I, I, I, P, F, P, SZ, P]
+    lib.attn_decode_batched_noalloc.restype = I
+    lib.attn_decode_batched_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, P, F, P]
     lib.kv_cache_scatter.restype = I
     lib.kv_cache_scatter.argtypes = [P, P, P, P, I, I, I, I, I, P, P, P]
     _lib = lib
@@ -133,6 +135,14 @@ def attn_decode_batched(q, k_cache, v_cache, o, M, n_heads, n_kv_heads, head_dim
     _check("attn_decode_batched", load().attn_decode_batched(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), M, n_heads, n_kv_heads, head_dim, max_len,
         _ptr(seq_lens), float(scale), _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def attn_decode_batched_noalloc(q, k_cache, v_cache, o, M, n_heads, n_kv_heads, head_dim, max_len,
+                                seq_lens, scale, stream=None):
+    """attn_decode_batched with the library's built-in scratch instead of a caller workspace."""
+    _check("attn_decode_batched_noalloc", load().attn_decode_batched_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), M, n_heads, n_kv_heads, head_dim, max_len,
+        _ptr(seq_lens), float(scale), _stream(stream)))
 
 
 def kv_cache_scatter(k_new, v_new, k_cache, v_cache, M, T, n_kv_heads, head_dim, max_len, start_pos,
