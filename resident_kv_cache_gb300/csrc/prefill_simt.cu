@@ -90,6 +90,4 @@ rkv_status launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream) {
     return check_launch("attn_prefill");
 }
 
-rkv_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) { return launch_prefill_simt(a, stream); }
-
 }  // namespace rkv

@@ -1,0 +1,504 @@
+// prefill_tc.cu -- fused flash-style prefill on the 5th-generation tensor core (sm_103a).
+//
+// Semantics: trueno-gpu 0.4.11 src/memory/resident/attention.rs,
+// fn batched_multihead_attention_optimized (interleaved [seq, n_heads*head_dim]
+// in and out, scale 1/sqrt(head_dim)) and trustformers-core 0.2.0
+// src/gpu_ops/cuda/oxicuda/attention.rs, fn attention_prefill_gpu_to_gpu
+// (causal: query i sees keys 0..=i; per head: scaled GEMM, causal softmax,
+// GEMM).  Here all of it is one kernel: heads are read in place, the score
+// tile never leaves tensor memory, and softmax is online (base 2).
+//
+// One CTA computes a 128-query tile of one (batch, head):
+//   warp 0       K producer: TMA (cp.async.bulk.tensor, 128-byte swizzle) of
+//                BN x D key tiles into an NK-stage ring, K-major for the MMA.
+//   warp 1       MMA issuer (one thread) and TMEM owner:
+//                  S_j  = Q . K_j^T   tcgen05.mma kind::tf32, A = Q from TMEM
+//                  O   += P_j . V_j   tcgen05.mma kind::tf32, A = P from TMEM
+//                S is double-buffered in TMEM so QK^T of block j+1 overlaps the
+//                softmax of block j.
+//   warps 2-5    softmax / epilogue, one thread per query row (TMEM lane):
+//                Q rows -> TMEM (pre-scaled by scale*log2e, rounded to TF32),
+//                then per block: S row from TMEM, mask, row max, lazy rescale
+//                (O is rescaled only when the running max grows by more than
+//                2^8), p = 2^(s - m) rounded to TF32 and written back over S,
+//                then O / l stored to the interleaved output row.
+//   warps 6-9    V transposer: tcgen05 kind::tf32 reads B only K-major, so V
+//                tiles are loaded with 16-byte loads, transposed in registers
+//                (4x4 blocks), rounded to TF32 and stored K-major (128-byte
+//                swizzle, conflict-free 16-byte stores) into an NV-stage ring.
+// Every mbarrier wait is time-bounded (see rkv_internal.cuh); a CTA that gives
+// up unwinds: it drains its own copies in flight, lets issued MMAs finish and
+// frees its TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "rkv_internal.cuh"
+#include "rkv_launch.h"
+
+namespace rkv {
+
+constexpr int kPfBM = 128;                    // query rows per CTA (TMEM lanes)
+constexpr int kPfThreads = 320;               // 10 warps
+constexpr int kPfSoftmaxWarp0 = 2;
+constexpr int kPfVWarp0 = 6;
+constexpr uint32_t kPfTmemCols = 512;
+constexpr uint32_t kColQ = 0, kColO = 128, kColS = 256;
+constexpr float kPfLog2e = 1.4426950408889634f;
+constexpr float kLazyRescale = 8.0f;          // log2 of the largest unnormalised p kept
+constexpr int kPfMinSmem = 120 * 1024;        // keeps one CTA per SM (TMEM is allocated whole)
+
+template <int D>
+struct PfCfg {
+    static constexpr int BN = D == 128 ? 64 : 128;          // keys per block
+    static constexpr int CH = D >= 32 ? 32 : D;             // floats per swizzled K row chunk
+    static constexpr int NCH = D / CH;
+    static constexpr int TILE = BN * D * 4;                 // bytes of one K or V^T tile
+    static constexpr int NK = D >= 64 ? 3 : 4;              // K stages
+    static constexpr int NV = D >= 64 ? 3 : 4;              // V^T stages
+    static constexpr uint32_t K_SWIZZLE = D >= 32 ? kSwizzle128B : kSwizzle64B;
+    static constexpr uint32_t K_ATOM = D >= 32 ? 1024 : 512; // 8 rows x swizzle span
+    // shared memory layout (offsets from a 1024-aligned base)
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + NK * TILE;
+    static constexpr int OFF_BAR = OFF_V + NV * TILE;
+    // barriers: k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_ready[2],
+    //           o_done, o_final, q_ready, drain
+    static constexpr int NBAR = 2 * NK + 2 * NV + 2 + 2 + 4;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;     // tmem base, abort flag
+    static constexpr int SMEM_USED = OFF_MISC + 16;
+    static constexpr int SMEM = (SMEM_USED + 1024 > kPfMinSmem ? SMEM_USED + 1024 : kPfMinSmem);
+    static_assert(SMEM <= 227 * 1024, "prefill shared memory budget");
+    static_assert(kColS + 2 * BN <= (int)kPfTmemCols && D <= 128, "TMEM budget");
+};
+
+struct PfBars {
+    uint32_t k_full, k_empty, v_full, v_empty, s_full, p_ready, o_done, o_final, q_ready, drain;
+};
+
+template <int NK, int NV>
+__device__ __forceinline__ PfBars pf_bars(uint32_t base) {
+    PfBars b;
+    b.k_full = base;
+    b.k_empty = b.k_full + 8 * NK;
+    b.v_full = b.k_empty + 8 * NK;
+    b.v_empty = b.v_full + 8 * NV;
+    b.s_full = b.v_empty + 8 * NV;
+    b.p_ready = b.s_full + 16;
+    b.o_done = b.p_ready + 16;
+    b.o_final = b.o_done + 8;
+    b.q_ready = b.o_final + 8;
+    b.drain = b.q_ready + 8;
+    return b;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPfThreads, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restrict__ q,
+                  const float* __restrict__ v, float* __restrict__ o, int B, int S, int H, int Hk,
+                  int causal, const int* __restrict__ seq_lens, float scale_log2, int n_qtiles,
+                  unsigned int* __restrict__ flags) {
+    using C = PfCfg<D>;
+    constexpr int BN = C::BN;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                           ~static_cast<uintptr_t>(1023));
+    const PfBars bar = pf_bars<C::NK, C::NV>(smem_addr(smem + C::OFF_BAR));
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int BH = B * H;
+    const int tile = n_qtiles - 1 - (int)(blockIdx.x / BH);   // heaviest causal tiles first
+    const int bh = (int)(blockIdx.x % BH);
+    const int b = bh / H, h = bh % H, g = h / (H / Hk);
+    const int q0 = tile * kPfBM;
+
+    int len = S;
+    if (seq_lens) {
+        len = __ldg(seq_lens + b);
+        if (len > S) { len = S; if (threadIdx.x == 0 && tile == n_qtiles - 1) atomicOr(flags, RKV_FLAG_LEN_CLAMPED); }
+        if (len < 0) { len = 0; if (threadIdx.x == 0 && tile == n_qtiles - 1) atomicOr(flags, RKV_FLAG_NEGATIVE_INPUT); }
+    }
+    // keys this tile needs: [0, kv_end)
+    const int kv_end = q0 >= len ? 0 : (causal ? min(len, q0 + kPfBM) : len);
+    const int nblk = (kv_end + BN - 1) / BN;
+    const int64_t q_row = (int64_t)H * D, kv_row = (int64_t)Hk * D;
+
+    // ------------------------------------------------------------------ setup
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), kPfTmemCols);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::NK; ++s) {
+            mbar_init(bar.k_full + 8 * s, 1);
+            mbar_init(bar.k_empty + 8 * s, 1);
+        }
+        for (int s = 0; s < C::NV; ++s) {
+            mbar_init(bar.v_full + 8 * s, 128);
+            mbar_init(bar.v_empty + 8 * s, 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar.s_full + 8 * s, 1);
+            mbar_init(bar.p_ready + 8 * s, 128);
+        }
+        mbar_init(bar.o_done, 1);
+        mbar_init(bar.o_final, 1);
+        mbar_init(bar.q_ready, 128);
+        mbar_init(bar.drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        prefetch_tmap(&tm_k);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (nblk > 0) {
+        if (warp == 0) {
+            // ============================================================ K producer
+            if (lane == 0) {
+                int issued = 0;
+                for (int j = 0; j < nblk; ++j) {
+                    const int s = j % C::NK;
+                    const uint32_t ph = (uint32_t)(j / C::NK) & 1u;
+                    if (!mbar_wait(bar.k_empty + 8 * s, ph ^ 1u, abort_flag, flags)) break;
+                    const uint32_t full = bar.k_full + 8 * s;
+                    mbar_arrive_expect_tx(full, C::TILE);
+                    const uint32_t dst = smem_addr(smem + C::OFF_K + s * C::TILE);
+#pragma unroll
+                    for (int c = 0; c < C::NCH; ++c)
+                        tma_load_3d(dst + c * BN * C::CH * 4, &tm_k, g * D + c * C::CH, j * BN, b, full);
+                    issued = j + 1;
+                }
+                if (*abort_flag) {   // unwinding: let issued copies land
+                    for (int j = max(0, issued - C::NK); j < issued; ++j)
+                        mbar_drain(bar.k_full + 8 * (j % C::NK), (uint32_t)(j / C::NK) & 1u, 100000000ull);
+                }
+            }
+        } else if (warp == 1) {
+            // ============================================================ MMA issuer
+            if (lane == 0) {
+                constexpr uint32_t id_qk = idesc_tf32(kPfBM, BN, false);
+                constexpr uint32_t id_pv = idesc_tf32(kPfBM, D, false);
+                bool ok = mbar_wait(bar.q_ready, 0, abort_flag, flags);
+                int issued_any = 0;
+                auto issue_qk = [&](int j) -> bool {
+                    const int s = j % C::NK;
+                    if (!mbar_wait(bar.k_full + 8 * s, (uint32_t)(j / C::NK) & 1u, abort_flag, flags)) return false;
+                    tc_fence_after();
+                    const uint32_t kbase = smem_addr(smem + C::OFF_K + s * C::TILE);
+                    const uint32_t d_tmem = tmem + kColS + (uint32_t)((j & 1) * BN);
+#pragma unroll
+                    for (int k = 0; k < D / 8; ++k) {
+                        const int c = k / (C::CH / 8), kk = k % (C::CH / 8);
+                        const uint64_t bdesc =
+                            smem_desc(kbase + c * BN * C::CH * 4 + kk * 32, 16, C::K_ATOM, C::K_SWIZZLE);
+                        mma_tf32_ts(d_tmem, tmem + kColQ + 8 * k, bdesc, id_qk, k > 0);
+                    }
+                    mma_commit(bar.s_full + 8 * (j & 1));
+                    mma_commit(bar.k_empty + 8 * s);
+                    issued_any = 1;
+                    return true;
+                };
+                if (ok) ok = issue_qk(0);
+                for (int j = 1; ok && j <= nblk; ++j) {
+                    if (j < nblk && !(ok = issue_qk(j))) break;
+                    // O += P_{j-1} V_{j-1}
+                    const int pj = j - 1;
+                    const int sv = pj % C::NV;
+                    if (!(ok = mbar_wait(bar.p_ready + 8 * (pj & 1), (uint32_t)(pj >> 1) & 1u, abort_flag, flags))) break;
+                    if (!(ok = mbar_wait(bar.v_full + 8 * sv, (uint32_t)(pj / C::NV) & 1u, abort_flag, flags))) break;
+                    tc_fence_after();
+                    const uint32_t vbase = smem_addr(smem + C::OFF_V + sv * C::TILE);
+                    const uint32_t a_tmem = tmem + kColS + (uint32_t)((pj & 1) * BN);
+#pragma unroll
+                    for (int k = 0; k < BN / 8; ++k) {
+                        // V^T tile: rows = d, 32 keys per 128-byte row, key chunks D*128 bytes apart
+                        const uint64_t bdesc =
+                            smem_desc(vbase + (k / 4) * (D * 128) + (k % 4) * 32, 16, 1024, kSwizzle128B);
+                        mma_tf32_ts(tmem + kColO, a_tmem + 8 * k, bdesc, id_pv, (pj > 0 || k > 0) ? 1u : 0u);
+                    }
+                    mma_commit(bar.o_done);
+                    mma_commit(bar.v_empty + 8 * sv);
+                }
+                if (ok) {
+                    mma_commit(bar.o_final);
+                } else if (issued_any) {   // unwinding: let issued MMAs finish before TMEM is freed
+                    mma_commit(bar.drain);
+                    mbar_drain(bar.drain, 0, 100000000ull);
+                }
+            }
+        } else if (warp >= kPfVWarp0) {
+            // ============================================================ V transposer
+            // Work item = (key quad aa, d quad dq): a 4x4 block of V.  Lanes take
+            // consecutive key quads (aa & 7 = lane & 7), so the eight 16-byte
+            // stores of a quarter-warp land in eight distinct swizzled chunks.
+            const int t = threadIdx.x - kPfVWarp0 * 32;          // 0..127
+            constexpr int AGROUPS = BN / 32;                     // groups of 8 key quads
+            constexpr int ITEMS = (BN / 4) * (D / 4);
+            constexpr int PER = ITEMS / 128;
+            static_assert(ITEMS % 128 == 0, "V transposer work split");
+            const float* vb = v + (int64_t)b * S * kv_row + (int64_t)g * D;
+            for (int j = 0; j < nblk; ++j) {
+                const int s = j % C::NV;
+                float4 x[PER][4];
+#pragma unroll
+                for (int it = 0; it < PER; ++it) {              // loads first, before the slot wait
+                    const int item = t + 128 * it;
+                    const int aa = ((item >> 3) % AGROUPS) * 8 + (item & 7);
+                    const int dq = (item >> 3) / AGROUPS;
+                    const int key0 = j * BN + aa * 4;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int key = key0 + r;
+                        x[it][r] = key < S ? __ldg(reinterpret_cast<const float4*>(vb + (int64_t)key * kv_row) + dq)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+                if (!mbar_wait(bar.v_empty + 8 * s, ((uint32_t)(j / C::NV) & 1u) ^ 1u, abort_flag, flags)) break;
+                unsigned char* vt = smem + C::OFF_V + s * C::TILE;
+#pragma unroll
+                for (int it = 0; it < PER; ++it) {
+                    const int item = t + 128 * it;
+                    const int aa = ((item >> 3) % AGROUPS) * 8 + (item & 7);
+                    const int dq = (item >> 3) / AGROUPS;
+                    const int kc = aa >> 3;                      // 32-key chunk of the V^T row
+                    const float4 c0 = x[it][0], c1 = x[it][1], c2 = x[it][2], c3 = x[it][3];
+                    const uint4 w[4] = {
+                        make_uint4(round_tf32(c0.x), round_tf32(c1.x), round_tf32(c2.x), round_tf32(c3.x)),
+                        make_uint4(round_tf32(c0.y), round_tf32(c1.y), round_tf32(c2.y), round_tf32(c3.y)),
+                        make_uint4(round_tf32(c0.z), round_tf32(c1.z), round_tf32(c2.z), round_tf32(c3.z)),
+                        make_uint4(round_tf32(c0.w), round_tf32(c1.w), round_tf32(c2.w), round_tf32(c3.w))};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int d = dq * 4 + i;
+                        const int off = kc * (D * 128) + d * 128 + (((aa & 7) ^ (d & 7)) << 4);
+                        *reinterpret_cast<uint4*>(vt + off) = w[i];
+                    }
+                }
+                fence_proxy_async();          // generic-proxy stores -> tensor-core reads
+                mbar_arrive(bar.v_full + 8 * s);
+            }
+        } else {
+            // ============================================================ softmax / epilogue
+            const int quad = warp & 3;                       // TMEM lane quadrant of this warp
+            const int r = quad * 32 + lane;                  // query row within the tile
+            const int qi = q0 + r;
+            const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+            // Q row -> TMEM (pre-scaled, rounded to TF32)
+            {
+                const float4* qp = reinterpret_cast<const float4*>(q + ((int64_t)b * S + qi) * q_row + (int64_t)h * D);
+                if constexpr (D >= 32) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t w[32];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            float4 t4 = qi < S ? __ldg(qp + c * 8 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            w[4 * e + 0] = round_tf32(t4.x * scale_log2);
+                            w[4 * e + 1] = round_tf32(t4.y * scale_log2);
+                            w[4 * e + 2] = round_tf32(t4.z * scale_log2);
+                            w[4 * e + 3] = round_tf32(t4.w * scale_log2);
+                        }
+                        tmem_st32(lane_base + kColQ + 32 * c, w);
+                    }
+                } else {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float4 t4 = qi < S ? __ldg(qp + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        w[4 * e + 0] = round_tf32(t4.x * scale_log2);
+                        w[4 * e + 1] = round_tf32(t4.y * scale_log2);
+                        w[4 * e + 2] = round_tf32(t4.z * scale_log2);
+                        w[4 * e + 3] = round_tf32(t4.w * scale_log2);
+                    }
+                    tmem_st16(lane_base + kColQ, w);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar.q_ready);
+            }
+            float m_run = -INFINITY, l_run = 0.0f;
+            bool ok = true;
+            const int key_lim = causal ? min(qi + 1, len) : len;   // keys visible to this row
+            for (int j = 0; j < nblk; ++j) {
+                ok = mbar_wait(bar.s_full + 8 * (j & 1), (uint32_t)(j >> 1) & 1u, abort_flag, flags);
+                if (!(ok = __all_sync(0xffffffffu, ok))) break;   // warp-uniform before TMEM access
+                tc_fence_after();
+                const uint32_t s_col = lane_base + kColS + (uint32_t)((j & 1) * BN);
+                float s[BN];
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t w[32];
+                    tmem_ld32(s_col + 32 * c, w);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(w[e]);
+                }
+                const int k0 = j * BN;
+                const int nvis = min(max(key_lim - k0, 0), BN);     // visible keys of this block
+                float m_blk = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < BN; ++e) {
+                    if (e >= nvis) s[e] = -INFINITY;
+                    m_blk = fmaxf(m_blk, s[e]);
+                }
+                const bool need = m_blk > m_run + kLazyRescale;
+                const float m_use = need ? m_blk : m_run;
+                const float alpha = need ? fast_exp2(m_run - m_blk) : 1.0f;
+                float lsum = 0.0f;
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float x = s[32 * c + e];
+                        const float p = (x == -INFINITY) ? 0.0f : fast_exp2(x - m_use);
+                        w[e] = round_tf32(p);
+                        lsum += __uint_as_float(w[e]);
+                    }
+                    tmem_st32(s_col + 32 * c, w);
+                }
+                l_run = l_run * alpha + lsum;
+                m_run = m_use;
+                tmem_wait_st();
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+                    // O holds blocks < j once PV_{j-1} completes; scale it by alpha
+                    ok = mbar_wait(bar.o_done, (uint32_t)(j - 1) & 1u, abort_flag, flags);
+                    if (!(ok = __all_sync(0xffffffffu, ok))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < (D + 31) / 32; ++c) {
+                        if constexpr (D >= 32) {
+                            uint32_t w[32];
+                            tmem_ld32(lane_base + kColO + 32 * c, w);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) * alpha);
+                            tmem_st32(lane_base + kColO + 32 * c, w);
+                        } else {
+                            uint32_t w[16];
+                            tmem_ld16(lane_base + kColO, w);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) * alpha);
+                            tmem_st16(lane_base + kColO, w);
+                        }
+                    }
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                mbar_arrive(bar.p_ready + 8 * (j & 1));
+            }
+            // ---------------------------------------------------------- epilogue
+            if (ok) ok = mbar_wait(bar.o_final, 0, abort_flag, flags);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                tc_fence_after();
+                const float inv = (qi < len && l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+                float4* op = reinterpret_cast<float4*>(o + ((int64_t)b * S + qi) * q_row + (int64_t)h * D);
+#pragma unroll
+                for (int c = 0; c < (D + 31) / 32; ++c) {
+                    if constexpr (D >= 32) {
+                        uint32_t w[32];
+                        tmem_ld32(lane_base + kColO + 32 * c, w);
+                        tmem_wait_ld();
+                        if (qi < S) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                op[c * 8 + e] = make_float4(__uint_as_float(w[4 * e]) * inv, __uint_as_float(w[4 * e + 1]) * inv,
+                                                            __uint_as_float(w[4 * e + 2]) * inv, __uint_as_float(w[4 * e + 3]) * inv);
+                        }
+                    } else {
+                        uint32_t w[16];
+                        tmem_ld16(lane_base + kColO, w);
+                        tmem_wait_ld();
+                        if (qi < S) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                op[e] = make_float4(__uint_as_float(w[4 * e]) * inv, __uint_as_float(w[4 * e + 1]) * inv,
+                                                    __uint_as_float(w[4 * e + 2]) * inv, __uint_as_float(w[4 * e + 3]) * inv);
+                        }
+                    }
+                }
+            }
+        }
+    } else if (warp >= kPfSoftmaxWarp0 && warp < kPfVWarp0) {
+        // no key is visible to any row of this tile: the rows are padding -> zeros
+        const int r = (warp & 3) * 32 + lane;
+        const int qi = q0 + r;
+        if (qi < S) {
+            float4* op = reinterpret_cast<float4*>(o + ((int64_t)b * S + qi) * q_row + (int64_t)h * D);
+#pragma unroll
+            for (int e = 0; e < D / 4; ++e) op[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kPfTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
+                cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+template <int D>
+static rkv_status launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
+    using C = PfCfg<D>;
+    auto encode = tensor_map_encoder();
+    if (!encode) return set_error(RKV_ERR_LAUNCH, "attn_prefill: cuTensorMapEncodeTiled unavailable");
+    CUtensorMap tm_k;
+    const cuuint64_t dims[3] = {(cuuint64_t)a.Hk * D, (cuuint64_t)a.S, (cuuint64_t)a.B};
+    const cuuint64_t strides[2] = {(cuuint64_t)a.Hk * D * 4, (cuuint64_t)a.S * a.Hk * D * 4};
+    const cuuint32_t box[3] = {(cuuint32_t)C::CH, (cuuint32_t)C::BN, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult cr = encode(&tm_k, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(a.k), dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         D >= 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return set_error(RKV_ERR_LAUNCH, "attn_prefill: tensor map encode failed (%d)", (int)cr);
+    auto kern = prefill_tc_kernel<D>;
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+            return check_launch("attn_prefill: shared-memory attribute");
+        attr_done[dev] = true;
+    }
+    const int n_qtiles = (a.S + kPfBM - 1) / kPfBM;
+    const int64_t grid = (int64_t)n_qtiles * a.B * a.H;
+    if (grid > 0x7FFFFFFF) return set_error(RKV_ERR_UNSUPPORTED, "attn_prefill: grid too large");
+    kern<<<(unsigned)grid, kPfThreads, C::SMEM, stream>>>(tm_k, a.q, a.v, a.o, a.B, a.S, a.H, a.Hk, a.causal ? 1 : 0,
+                                                           a.seq_lens, a.scale * kPfLog2e, n_qtiles, a.flags);
+    return check_launch("attn_prefill");
+}
+
+rkv_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+    switch (a.D) {
+        case 16: return launch_prefill_tc_t<16>(a, stream);
+        case 32: return launch_prefill_tc_t<32>(a, stream);
+        case 64: return launch_prefill_tc_t<64>(a, stream);
+        case 128: return launch_prefill_tc_t<128>(a, stream);
+    }
+    return set_error(RKV_ERR_UNSUPPORTED, "attn_prefill: head_dim %d", a.D);
+}
+
+}  // namespace rkv
