@@ -42,7 +42,7 @@ constexpr int kPfThreads = 320;               // 10 warps
 constexpr int kPfSoftmaxWarp0 = 2;
 constexpr int kPfVWarp0 = 6;
 constexpr uint32_t kPfTmemCols = 512;
-constexpr uint32_t kColQ = 0, kColO = 128, kColS = 256;
+constexpr uint32_t kColQ = 0, kColO = 128, kColS = 256;   // TMEM column bases
 constexpr float kPfLog2e = 1.4426950408889634f;
 constexpr float kLazyRescale = 8.0f;          // log2 of the largest unnormalised p kept
 constexpr int kPfMinSmem = 120 * 1024;        // keeps one CTA per SM (TMEM is allocated whole)
@@ -55,24 +55,32 @@ struct PfCfg {
     static constexpr int TILE = BN * D * 4;                 // bytes of one K or V^T tile
     static constexpr int NK = D >= 64 ? 3 : 4;              // K stages
     static constexpr int NV = D >= 64 ? 3 : 4;              // V^T stages
+    // The tensor core needs ~100 cycles per MMA that accumulates into the result of the
+    // previous one, so long K chains are latency-bound.  D = 128: QK^T is split over the
+    // two halves of D into two accumulators (S = S_a + S_b).  D <= 64: PV is split over
+    // even/odd key steps into two accumulators (O = O_a + O_b).
+    static constexpr int QK_SPLIT = D == 128 ? 2 : 1;
+    static constexpr int PV_SPLIT = D <= 64 ? 2 : 1;
+    static constexpr int S_BUF = BN * QK_SPLIT;            // TMEM columns of one S buffer
     static constexpr uint32_t K_SWIZZLE = D >= 32 ? kSwizzle128B : kSwizzle64B;
     static constexpr uint32_t K_ATOM = D >= 32 ? 1024 : 512; // 8 rows x swizzle span
     // shared memory layout (offsets from a 1024-aligned base)
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + NK * TILE;
     static constexpr int OFF_BAR = OFF_V + NV * TILE;
-    // barriers: k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_ready[2],
-    //           o_done, o_final, q_ready, drain
-    static constexpr int NBAR = 2 * NK + 2 * NV + 2 + 2 + 4;
+    // barriers: k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], v_loaded[NV], s_full[2],
+    //           p_ready[2], o_done, o_final, q_ready, drain
+    static constexpr int NBAR = 2 * NK + 3 * NV + 2 + 2 + 4;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;     // tmem base, abort flag
     static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM = (SMEM_USED + 1024 > kPfMinSmem ? SMEM_USED + 1024 : kPfMinSmem);
     static_assert(SMEM <= 227 * 1024, "prefill shared memory budget");
-    static_assert(kColS + 2 * BN <= (int)kPfTmemCols && D <= 128, "TMEM budget");
+    static_assert(kColS + 2 * S_BUF <= (int)kPfTmemCols && kColO + PV_SPLIT * D <= kColS && D <= 128,
+                  "TMEM budget");
 };
 
 struct PfBars {
-    uint32_t k_full, k_empty, v_full, v_empty, s_full, p_ready, o_done, o_final, q_ready, drain;
+    uint32_t k_full, k_empty, v_full, v_empty, v_loaded, s_full, p_ready, o_done, o_final, q_ready, drain;
 };
 
 template <int NK, int NV>
@@ -82,7 +90,8 @@ __device__ __forceinline__ PfBars pf_bars(uint32_t base) {
     b.k_empty = b.k_full + 8 * NK;
     b.v_full = b.k_empty + 8 * NK;
     b.v_empty = b.v_full + 8 * NV;
-    b.s_full = b.v_empty + 8 * NV;
+    b.v_loaded = b.v_empty + 8 * NV;
+    b.s_full = b.v_loaded + 8 * NV;
     b.p_ready = b.s_full + 16;
     b.o_done = b.p_ready + 16;
     b.o_final = b.o_done + 8;
@@ -93,8 +102,8 @@ __device__ __forceinline__ PfBars pf_bars(uint32_t base) {
 
 template <int D>
 __global__ void __launch_bounds__(kPfThreads, 1)
-prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restrict__ q,
-                  const float* __restrict__ v, float* __restrict__ o, int B, int S, int H, int Hk,
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const float* __restrict__ q, float* __restrict__ o, int B, int S, int H, int Hk,
                   int causal, const int* __restrict__ seq_lens, float scale_log2, int n_qtiles,
                   unsigned int* __restrict__ flags) {
     using C = PfCfg<D>;
@@ -122,7 +131,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restr
     // keys this tile needs: [0, kv_end)
     const int kv_end = q0 >= len ? 0 : (causal ? min(len, q0 + kPfBM) : len);
     const int nblk = (kv_end + BN - 1) / BN;
-    const int64_t q_row = (int64_t)H * D, kv_row = (int64_t)Hk * D;
+    const int64_t q_row = (int64_t)H * D;
 
     // ------------------------------------------------------------------ setup
     if (warp == 1) {
@@ -137,6 +146,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restr
         for (int s = 0; s < C::NV; ++s) {
             mbar_init(bar.v_full + 8 * s, 128);
             mbar_init(bar.v_empty + 8 * s, 1);
+            mbar_init(bar.v_loaded + 8 * s, 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar.s_full + 8 * s, 1);
@@ -149,6 +159,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restr
         *abort_flag = 0;
         fence_barrier_init();
         prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
     }
     tc_fence_before();
     __syncthreads();
@@ -157,24 +168,31 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restr
 
     if (nblk > 0) {
         if (warp == 0) {
-            // ============================================================ K producer
-            if (lane == 0) {
+            // ============================================================ K and V producers
+            // lane 0 streams K tiles, lane 16 streams V tiles (both by TMA, same box shape)
+            if (lane == 0 || lane == 16) {
+                const bool is_k = lane == 0;
+                const int NS = is_k ? C::NK : C::NV;
+                const uint32_t empty0 = is_k ? bar.k_empty : bar.v_empty;
+                const uint32_t full0 = is_k ? bar.k_full : bar.v_loaded;
+                const int off0 = is_k ? C::OFF_K : C::OFF_V;
+                const void* tm = is_k ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
                 int issued = 0;
                 for (int j = 0; j < nblk; ++j) {
-                    const int s = j % C::NK;
-                    const uint32_t ph = (uint32_t)(j / C::NK) & 1u;
-                    if (!mbar_wait(bar.k_empty + 8 * s, ph ^ 1u, abort_flag, flags)) break;
-                    const uint32_t full = bar.k_full + 8 * s;
+                    const int s = j % NS;
+                    const uint32_t ph = (uint32_t)(j / NS) & 1u;
+                    if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag, flags)) break;
+                    const uint32_t full = full0 + 8 * s;
                     mbar_arrive_expect_tx(full, C::TILE);
-                    const uint32_t dst = smem_addr(smem + C::OFF_K + s * C::TILE);
+                    const uint32_t dst = smem_addr(smem + off0 + s * C::TILE);
 #pragma unroll
                     for (int c = 0; c < C::NCH; ++c)
-                        tma_load_3d(dst + c * BN * C::CH * 4, &tm_k, g * D + c * C::CH, j * BN, b, full);
+                        tma_load_3d(dst + c * BN * C::CH * 4, tm, g * D + c * C::CH, j * BN, b, full);
                     issued = j + 1;
                 }
                 if (*abort_flag) {   // unwinding: let issued copies land
-                    for (int j = max(0, issued - C::NK); j < issued; ++j)
-                        mbar_drain(bar.k_full + 8 * (j % C::NK), (uint32_t)(j / C::NK) & 1u, 100000000ull);
+                    for (int j = max(0, issued - NS); j < issued; ++j)
+                        mbar_drain(full0 + 8 * (j % NS), (uint32_t)(j / NS) & 1u, 100000000ull);
                 }
             }
         } else if (warp == 1) {
@@ -184,18 +202,28 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restr
                 constexpr uint32_t id_pv = idesc_tf32(kPfBM, D, false);
                 bool ok = mbar_wait(bar.q_ready, 0, abort_flag, flags);
                 int issued_any = 0;
+                // Descriptors are built once per ring stage; a k step only adds its byte
+                // offset (>> 4) to the start-address field, which cannot carry out of it
+                // (shared addresses are below 2^18).  Keeping the issue loop lean matters:
+                // one thread must issue an MMA every ~32-64 cycles to keep the tensor core fed.
+                const uint64_t kdesc0 = smem_desc(smem_addr(smem + C::OFF_K), 16, C::K_ATOM, C::K_SWIZZLE);
+                const uint64_t vdesc0 = smem_desc(smem_addr(smem + C::OFF_V), 16, 1024, kSwizzle128B);
                 auto issue_qk = [&](int j) -> bool {
                     const int s = j % C::NK;
                     if (!mbar_wait(bar.k_full + 8 * s, (uint32_t)(j / C::NK) & 1u, abort_flag, flags)) return false;
                     tc_fence_after();
-                    const uint32_t kbase = smem_addr(smem + C::OFF_K + s * C::TILE);
-                    const uint32_t d_tmem = tmem + kColS + (uint32_t)((j & 1) * BN);
+                    const uint64_t kd = kdesc0 + (uint64_t)(s * (C::TILE >> 4));
+                    const uint32_t d_tmem = tmem + kColS + (uint32_t)((j & 1) * C::S_BUF);
+                    constexpr int KSTEPS = D / 8 / C::QK_SPLIT;     // steps per accumulator chain
 #pragma unroll
-                    for (int k = 0; k < D / 8; ++k) {
-                        const int c = k / (C::CH / 8), kk = k % (C::CH / 8);
-                        const uint64_t bdesc =
-                            smem_desc(kbase + c * BN * C::CH * 4 + kk * 32, 16, C::K_ATOM, C::K_SWIZZLE);
-                        mma_tf32_ts(d_tmem, tmem + kColQ + 8 * k, bdesc, id_qk, k > 0);
+                    for (int ks = 0; ks < KSTEPS; ++ks) {
+#pragma unroll
+                        for (int part = 0; part < C::QK_SPLIT; ++part) {   // interleave the chains
+                            const int k = part * KSTEPS + ks;
+                            const int c = k / (C::CH / 8), kk = k % (C::CH / 8);
+                            const uint64_t bdesc = kd + (uint64_t)((c * BN * C::CH * 4 + kk * 32) >> 4);
+                            mma_tf32_ts(d_tmem + part * BN, tmem + kColQ + 8 * k, bdesc, id_qk, ks > 0 ? 1u : 0u);
+                        }
                     }
                     mma_commit(bar.s_full + 8 * (j & 1));
                     mma_commit(bar.k_empty + 8 * s);
@@ -211,14 +239,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restr
                     if (!(ok = mbar_wait(bar.p_ready + 8 * (pj & 1), (uint32_t)(pj >> 1) & 1u, abort_flag, flags))) break;
                     if (!(ok = mbar_wait(bar.v_full + 8 * sv, (uint32_t)(pj / C::NV) & 1u, abort_flag, flags))) break;
                     tc_fence_after();
-                    const uint32_t vbase = smem_addr(smem + C::OFF_V + sv * C::TILE);
-                    const uint32_t a_tmem = tmem + kColS + (uint32_t)((pj & 1) * BN);
+                    const uint64_t vd = vdesc0 + (uint64_t)(sv * (C::TILE >> 4));
+                    const uint32_t a_tmem = tmem + kColS + (uint32_t)((pj & 1) * C::S_BUF);
+                    const uint32_t first = pj > 0 ? 1u : 0u;
 #pragma unroll
                     for (int k = 0; k < BN / 8; ++k) {
                         // V^T tile: rows = d, 32 keys per 128-byte row, key chunks D*128 bytes apart
-                        const uint64_t bdesc =
-                            smem_desc(vbase + (k / 4) * (D * 128) + (k % 4) * 32, 16, 1024, kSwizzle128B);
-                        mma_tf32_ts(tmem + kColO, a_tmem + 8 * k, bdesc, id_pv, (pj > 0 || k > 0) ? 1u : 0u);
+                        const uint64_t bdesc = vd + (uint64_t)(((k / 4) * (D * 128) + (k % 4) * 32) >> 4);
+                        const int part = k % C::PV_SPLIT;
+                        mma_tf32_ts(tmem + kColO + part * D, a_tmem + 8 * k, bdesc, id_pv,
+                                    k >= C::PV_SPLIT ? 1u : first);
                     }
                     mma_commit(bar.o_done);
                     mma_commit(bar.v_empty + 8 * sv);
@@ -232,38 +262,51 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restr
             }
         } else if (warp >= kPfVWarp0) {
             // ============================================================ V transposer
-            // Work item = (key quad aa, d quad dq): a 4x4 block of V.  Lanes take
-            // consecutive key quads (aa & 7 = lane & 7), so the eight 16-byte
-            // stores of a quarter-warp land in eight distinct swizzled chunks.
-            const int t = threadIdx.x - kPfVWarp0 * 32;          // 0..127
-            constexpr int AGROUPS = BN / 32;                     // groups of 8 key quads
-            constexpr int ITEMS = (BN / 4) * (D / 4);
-            constexpr int PER = ITEMS / 128;
-            static_assert(ITEMS % 128 == 0, "V transposer work split");
-            const float* vb = v + (int64_t)b * S * kv_row + (int64_t)g * D;
+            // V tiles arrive by TMA in the same swizzled layout as K (rows = keys).  The
+            // transposer rewrites each slot in place as V^T: work item = (key quad aa,
+            // d quad dq), a 4x4 block read with four 16-byte loads and written as four
+            // 16-byte rows of V^T.  Lane numbering puts 4 consecutive key quads x 2 d
+            // quads (D = 16: 8 key quads x 1) in each quarter-warp, so its eight V^T
+            // stores hit eight distinct 128-byte-swizzle chunks: no conflicts.
+            const int wv = warp - kPfVWarp0;                      // 0..3
+            constexpr int LDQ = D / 4 < 8 ? D / 4 : 8;           // lanes along d quads
+            constexpr int LAA = 32 / LDQ;                        // lanes along key quads
+            constexpr int GA = (BN / 4) / LAA;                   // lane groups along keys
+            constexpr int GD = (D / 4) / LDQ;                    // lane groups along d
+            constexpr int PER = GA * GD / 4;                     // groups per warp
+            static_assert(GA * GD % 4 == 0 && PER >= 1, "V transposer work split");
+            const int aa_lo = lane % LAA, dq_lo = lane / LAA;
+            // Byte offset of V[key][d] in a TMA-staged tile (box {CH floats, BN keys} per
+            // d chunk, swizzled: 16-byte chunk index XOR key bits).
+            auto staged = [](int key, int dq) -> int {
+                if constexpr (D >= 32)
+                    return (dq >> 3) * (BN * 128) + key * 128 + (((dq & 7) ^ (key & 7)) << 4);
+                else
+                    return key * 64 + (((dq & 3) ^ ((key >> 1) & 3)) << 4);
+            };
             for (int j = 0; j < nblk; ++j) {
                 const int s = j % C::NV;
+                unsigned char* vt = smem + C::OFF_V + s * C::TILE;
+                if (!mbar_wait(bar.v_loaded + 8 * s, (uint32_t)(j / C::NV) & 1u, abort_flag, flags)) break;
                 float4 x[PER][4];
 #pragma unroll
-                for (int it = 0; it < PER; ++it) {              // loads first, before the slot wait
-                    const int item = t + 128 * it;
-                    const int aa = ((item >> 3) % AGROUPS) * 8 + (item & 7);
-                    const int dq = (item >> 3) / AGROUPS;
-                    const int key0 = j * BN + aa * 4;
+                for (int it = 0; it < PER; ++it) {
+                    const int G = it * 4 + wv;
+                    const int aa = (G % GA) * LAA + aa_lo;
+                    const int dq = (G / GA) * LDQ + dq_lo;
 #pragma unroll
                     for (int r = 0; r < 4; ++r) {
-                        const int key = key0 + r;
-                        x[it][r] = key < S ? __ldg(reinterpret_cast<const float4*>(vb + (int64_t)key * kv_row) + dq)
-                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                        const int key = aa * 4 + r;
+                        // keys past the sequence end were zero-filled by the copy engine
+                        x[it][r] = *reinterpret_cast<const float4*>(vt + staged(key, dq));
                     }
                 }
-                if (!mbar_wait(bar.v_empty + 8 * s, ((uint32_t)(j / C::NV) & 1u) ^ 1u, abort_flag, flags)) break;
-                unsigned char* vt = smem + C::OFF_V + s * C::TILE;
+                named_barrier(2, 128);        // every thread has read its blocks: rewrite in place
 #pragma unroll
                 for (int it = 0; it < PER; ++it) {
-                    const int item = t + 128 * it;
-                    const int aa = ((item >> 3) % AGROUPS) * 8 + (item & 7);
-                    const int dq = (item >> 3) / AGROUPS;
+                    const int G = it * 4 + wv;
+                    const int aa = (G % GA) * LAA + aa_lo;
+                    const int dq = (G / GA) * LDQ + dq_lo;
                     const int kc = aa >> 3;                      // 32-key chunk of the V^T row
                     const float4 c0 = x[it][0], c1 = x[it][1], c2 = x[it][2], c3 = x[it][3];
                     const uint4 w[4] = {
@@ -327,28 +370,44 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restr
                 ok = mbar_wait(bar.s_full + 8 * (j & 1), (uint32_t)(j >> 1) & 1u, abort_flag, flags);
                 if (!(ok = __all_sync(0xffffffffu, ok))) break;   // warp-uniform before TMEM access
                 tc_fence_after();
-                const uint32_t s_col = lane_base + kColS + (uint32_t)((j & 1) * BN);
+                const uint32_t s_col = lane_base + kColS + (uint32_t)((j & 1) * C::S_BUF);
                 float s[BN];
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t w[32];
                     tmem_ld32(s_col + 32 * c, w);
-                    tmem_wait_ld();
+                    if constexpr (C::QK_SPLIT == 2) {
+                        uint32_t w2[32];
+                        tmem_ld32(s_col + BN + 32 * c, w2);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(w[e]);
+                        for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(w[e]) + __uint_as_float(w2[e]);
+                    } else {
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(w[e]);
+                    }
                 }
                 const int k0 = j * BN;
                 const int nvis = min(max(key_lim - k0, 0), BN);     // visible keys of this block
-                float m_blk = -INFINITY;
+                if (__any_sync(0xffffffffu, nvis < BN)) {
 #pragma unroll
-                for (int e = 0; e < BN; ++e) {
-                    if (e >= nvis) s[e] = -INFINITY;
-                    m_blk = fmaxf(m_blk, s[e]);
+                    for (int e = 0; e < BN; ++e)
+                        if (e >= nvis) s[e] = -INFINITY;
                 }
+                float mx[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) mx[t] = s[t];
+#pragma unroll
+                for (int e = 8; e < BN; ++e) mx[e & 7] = fmaxf(mx[e & 7], s[e]);
+                const float m_blk = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                          fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
                 const bool need = m_blk > m_run + kLazyRescale;
                 const float m_use = need ? m_blk : m_run;
                 const float alpha = need ? fast_exp2(m_run - m_blk) : 1.0f;
-                float lsum = 0.0f;
+                // p = 2^(s - m); the tensor core truncates f32 operands to TF32, so p is
+                // truncated here too and the row sum is taken over exactly those values
+                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t w[32];
@@ -356,11 +415,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restr
                     for (int e = 0; e < 32; ++e) {
                         const float x = s[32 * c + e];
                         const float p = (x == -INFINITY) ? 0.0f : fast_exp2(x - m_use);
-                        w[e] = round_tf32(p);
-                        lsum += __uint_as_float(w[e]);
+                        w[e] = __float_as_uint(p) & 0xFFFFE000u;
+                        ls[e & 7] += __uint_as_float(w[e]);
                     }
                     tmem_st32(s_col + 32 * c, w);
                 }
+                const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
                 l_run = l_run * alpha + lsum;
                 m_run = m_use;
                 tmem_wait_st();
@@ -370,7 +430,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restr
                     if (!(ok = __all_sync(0xffffffffu, ok))) break;
                     tc_fence_after();
 #pragma unroll
-                    for (int c = 0; c < (D + 31) / 32; ++c) {
+                    for (int c = 0; c < C::PV_SPLIT * ((D + 31) / 32); ++c) {
                         if constexpr (D >= 32) {
                             uint32_t w[32];
                             tmem_ld32(lane_base + kColO + 32 * c, w);
@@ -380,11 +440,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restr
                             tmem_st32(lane_base + kColO + 32 * c, w);
                         } else {
                             uint32_t w[16];
-                            tmem_ld16(lane_base + kColO, w);
+                            tmem_ld16(lane_base + kColO + 16 * c, w);
                             tmem_wait_ld();
 #pragma unroll
                             for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) * alpha);
-                            tmem_st16(lane_base + kColO, w);
+                            tmem_st16(lane_base + kColO + 16 * c, w);
                         }
                     }
                     tmem_wait_st();
@@ -404,7 +464,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restr
                     if constexpr (D >= 32) {
                         uint32_t w[32];
                         tmem_ld32(lane_base + kColO + 32 * c, w);
-                        tmem_wait_ld();
+                        if constexpr (C::PV_SPLIT == 2) {
+                            uint32_t w2[32];
+                            tmem_ld32(lane_base + kColO + D + 32 * c, w2);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) + __uint_as_float(w2[e]));
+                        } else {
+                            tmem_wait_ld();
+                        }
                         if (qi < S) {
 #pragma unroll
                             for (int e = 0; e < 8; ++e)
@@ -412,9 +480,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const float* __restr
                                                             __uint_as_float(w[4 * e + 2]) * inv, __uint_as_float(w[4 * e + 3]) * inv);
                         }
                     } else {
-                        uint32_t w[16];
+                        uint32_t w[16], w2[16];
                         tmem_ld16(lane_base + kColO, w);
+                        tmem_ld16(lane_base + kColO + D, w2);     // D = 16 always splits PV
                         tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) + __uint_as_float(w2[e]));
                         if (qi < S) {
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
@@ -464,15 +535,19 @@ static rkv_status launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream)
     using C = PfCfg<D>;
     auto encode = tensor_map_encoder();
     if (!encode) return set_error(RKV_ERR_LAUNCH, "attn_prefill: cuTensorMapEncodeTiled unavailable");
-    CUtensorMap tm_k;
+    CUtensorMap tm_k, tm_v;
     const cuuint64_t dims[3] = {(cuuint64_t)a.Hk * D, (cuuint64_t)a.S, (cuuint64_t)a.B};
     const cuuint64_t strides[2] = {(cuuint64_t)a.Hk * D * 4, (cuuint64_t)a.S * a.Hk * D * 4};
     const cuuint32_t box[3] = {(cuuint32_t)C::CH, (cuuint32_t)C::BN, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapSwizzle sw = D >= 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     CUresult cr = encode(&tm_k, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(a.k), dims, strides, box,
-                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         D >= 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr == CUDA_SUCCESS)
+        cr = encode(&tm_v, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(a.v), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return set_error(RKV_ERR_LAUNCH, "attn_prefill: tensor map encode failed (%d)", (int)cr);
     auto kern = prefill_tc_kernel<D>;
     static bool attr_done[64] = {false};
@@ -486,7 +561,7 @@ static rkv_status launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream)
     const int n_qtiles = (a.S + kPfBM - 1) / kPfBM;
     const int64_t grid = (int64_t)n_qtiles * a.B * a.H;
     if (grid > 0x7FFFFFFF) return set_error(RKV_ERR_UNSUPPORTED, "attn_prefill: grid too large");
-    kern<<<(unsigned)grid, kPfThreads, C::SMEM, stream>>>(tm_k, a.q, a.v, a.o, a.B, a.S, a.H, a.Hk, a.causal ? 1 : 0,
+    kern<<<(unsigned)grid, kPfThreads, C::SMEM, stream>>>(tm_k, tm_v, a.q, a.o, a.B, a.S, a.H, a.Hk, a.causal ? 1 : 0,
                                                            a.seq_lens, a.scale * kPfLog2e, n_qtiles, a.flags);
     return check_launch("attn_prefill");
 }

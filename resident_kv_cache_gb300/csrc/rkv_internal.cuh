@@ -47,6 +47,14 @@ __device__ __forceinline__ uint32_t round_tf32(float x) {
     return r;
 }
 
+// Round an f32 to the nearest TF32 value (ties away from zero) with integer ops:
+// add half a TF32 ulp to the magnitude bits and clear the 13 low mantissa bits.
+// Inf and NaN are passed through unchanged.
+__device__ __forceinline__ uint32_t round_tf32_int(float x) {
+    const uint32_t u = __float_as_uint(x);
+    return (u & 0x7FFFFFFFu) < 0x7F800000u ? ((u + 0x1000u) & 0xFFFFE000u) : u;
+}
+
 // Named barrier over `nthreads` threads (id 0 is __syncthreads).
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
