@@ -63,14 +63,17 @@ struct PfCfg {
     static constexpr int PV_SPLIT = D <= 64 ? 2 : 1;
     static constexpr int S_BUF = BN * QK_SPLIT;            // TMEM columns of one S buffer
     static constexpr uint32_t K_SWIZZLE = D >= 32 ? kSwizzle128B : kSwizzle64B;
+    // Q arrives by TMA into V ring slots 1 .. QSLOTS (free until V blocks 1.. are loaded)
+    static constexpr int QSLOTS = kPfBM / BN;
+    static_assert(1 + QSLOTS <= NV, "Q staging slots");
     static constexpr uint32_t K_ATOM = D >= 32 ? 1024 : 512; // 8 rows x swizzle span
     // shared memory layout (offsets from a 1024-aligned base)
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + NK * TILE;
     static constexpr int OFF_BAR = OFF_V + NV * TILE;
     // barriers: k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], v_loaded[NV], s_full[2],
-    //           p_ready[2], o_done, o_final, q_ready, drain
-    static constexpr int NBAR = 2 * NK + 3 * NV + 2 + 2 + 4;
+    //           p_ready[2], o_done, o_final, q_ready, drain, q_loaded
+    static constexpr int NBAR = 2 * NK + 3 * NV + 2 + 2 + 5;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;     // tmem base, abort flag
     static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM = (SMEM_USED + 1024 > kPfMinSmem ? SMEM_USED + 1024 : kPfMinSmem);
@@ -80,7 +83,7 @@ struct PfCfg {
 };
 
 struct PfBars {
-    uint32_t k_full, k_empty, v_full, v_empty, v_loaded, s_full, p_ready, o_done, o_final, q_ready, drain;
+    uint32_t k_full, k_empty, v_full, v_empty, v_loaded, s_full, p_ready, o_done, o_final, q_ready, drain, q_loaded;
 };
 
 template <int NK, int NV>
@@ -97,13 +100,14 @@ __device__ __forceinline__ PfBars pf_bars(uint32_t base) {
     b.o_final = b.o_done + 8;
     b.q_ready = b.o_final + 8;
     b.drain = b.q_ready + 8;
+    b.q_loaded = b.drain + 8;
     return b;
 }
 
 template <int D>
 __global__ void __launch_bounds__(kPfThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const float* __restrict__ q, float* __restrict__ o, int B, int S, int H, int Hk,
+                  const __grid_constant__ CUtensorMap tm_q, float* __restrict__ o, int B, int S, int H, int Hk,
                   int causal, const int* __restrict__ seq_lens, float scale_log2, int n_qtiles,
                   unsigned int* __restrict__ flags) {
     using C = PfCfg<D>;
@@ -156,10 +160,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         mbar_init(bar.o_final, 1);
         mbar_init(bar.q_ready, 128);
         mbar_init(bar.drain, 1);
+        mbar_init(bar.q_loaded, 1);
         *abort_flag = 0;
         fence_barrier_init();
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_q);
     }
     tc_fence_before();
     __syncthreads();
@@ -177,10 +183,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const uint32_t full0 = is_k ? bar.k_full : bar.v_loaded;
                 const int off0 = is_k ? C::OFF_K : C::OFF_V;
                 const void* tm = is_k ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
+                bool q_issued = false;
+                if (is_k) {       // the query tile, staged in V slots 1 .. QSLOTS
+                    mbar_arrive_expect_tx(bar.q_loaded, kPfBM * D * 4);
+                    const uint32_t qdst = smem_addr(smem + C::OFF_V + C::TILE);
+#pragma unroll
+                    for (int c = 0; c < C::NCH; ++c)
+                        tma_load_3d(qdst + c * kPfBM * C::CH * 4, &tm_q, h * D + c * C::CH, q0, b, bar.q_loaded);
+                    q_issued = true;
+                }
                 int issued = 0;
                 for (int j = 0; j < nblk; ++j) {
                     const int s = j % NS;
                     const uint32_t ph = (uint32_t)(j / NS) & 1u;
+                    if (!is_k && j == 1 && !mbar_wait(bar.q_ready, 0, abort_flag, flags)) break;   // Q consumed
                     if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag, flags)) break;
                     const uint32_t full = full0 + 8 * s;
                     mbar_arrive_expect_tx(full, C::TILE);
@@ -193,6 +209,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 if (*abort_flag) {   // unwinding: let issued copies land
                     for (int j = max(0, issued - NS); j < issued; ++j)
                         mbar_drain(full0 + 8 * (j % NS), (uint32_t)(j / NS) & 1u, 100000000ull);
+                    if (q_issued) mbar_drain(bar.q_loaded, 0, 100000000ull);
                 }
             }
         } else if (warp == 1) {
@@ -330,36 +347,47 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             const int r = quad * 32 + lane;                  // query row within the tile
             const int qi = q0 + r;
             const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-            // Q row -> TMEM (pre-scaled, rounded to TF32)
+            // Q row -> TMEM (pre-scaled, rounded to TF32), read from the TMA-staged tile
             {
-                const float4* qp = reinterpret_cast<const float4*>(q + ((int64_t)b * S + qi) * q_row + (int64_t)h * D);
-                if constexpr (D >= 32) {
+                bool qok = mbar_wait(bar.q_loaded, 0, abort_flag, flags);
+                qok = __all_sync(0xffffffffu, qok);
+                const unsigned char* qs = smem + C::OFF_V + C::TILE;
+                auto qv = [&](int dq) -> float4 {     // Q[r][4dq .. 4dq+3] in the swizzled staging
+                    if constexpr (D >= 32)
+                        return *reinterpret_cast<const float4*>(qs + (dq >> 3) * (kPfBM * 128) + r * 128 +
+                                                                (((dq & 7) ^ (r & 7)) << 4));
+                    else
+                        return *reinterpret_cast<const float4*>(qs + r * 64 + (((dq & 3) ^ ((r >> 1) & 3)) << 4));
+                };
+                if (qok) {
+                    if constexpr (D >= 32) {
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t w[32];
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t w[32];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            float4 t4 = qi < S ? __ldg(qp + c * 8 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            for (int e = 0; e < 8; ++e) {
+                                const float4 t4 = qv(c * 8 + e);
+                                w[4 * e + 0] = round_tf32(t4.x * scale_log2);
+                                w[4 * e + 1] = round_tf32(t4.y * scale_log2);
+                                w[4 * e + 2] = round_tf32(t4.z * scale_log2);
+                                w[4 * e + 3] = round_tf32(t4.w * scale_log2);
+                            }
+                            tmem_st32(lane_base + kColQ + 32 * c, w);
+                        }
+                    } else {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float4 t4 = qv(e);
                             w[4 * e + 0] = round_tf32(t4.x * scale_log2);
                             w[4 * e + 1] = round_tf32(t4.y * scale_log2);
                             w[4 * e + 2] = round_tf32(t4.z * scale_log2);
                             w[4 * e + 3] = round_tf32(t4.w * scale_log2);
                         }
-                        tmem_st32(lane_base + kColQ + 32 * c, w);
+                        tmem_st16(lane_base + kColQ, w);
                     }
-                } else {
-                    uint32_t w[16];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float4 t4 = qi < S ? __ldg(qp + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-                        w[4 * e + 0] = round_tf32(t4.x * scale_log2);
-                        w[4 * e + 1] = round_tf32(t4.y * scale_log2);
-                        w[4 * e + 2] = round_tf32(t4.z * scale_log2);
-                        w[4 * e + 3] = round_tf32(t4.w * scale_log2);
-                    }
-                    tmem_st16(lane_base + kColQ, w);
+                    tmem_wait_st();
                 }
-                tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar.q_ready);
             }
@@ -535,7 +563,7 @@ static rkv_status launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream)
     using C = PfCfg<D>;
     auto encode = tensor_map_encoder();
     if (!encode) return set_error(RKV_ERR_LAUNCH, "attn_prefill: cuTensorMapEncodeTiled unavailable");
-    CUtensorMap tm_k, tm_v;
+    CUtensorMap tm_k, tm_v, tm_q;
     const cuuint64_t dims[3] = {(cuuint64_t)a.Hk * D, (cuuint64_t)a.S, (cuuint64_t)a.B};
     const cuuint64_t strides[2] = {(cuuint64_t)a.Hk * D * 4, (cuuint64_t)a.S * a.Hk * D * 4};
     const cuuint32_t box[3] = {(cuuint32_t)C::CH, (cuuint32_t)C::BN, 1};
@@ -548,6 +576,14 @@ static rkv_status launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream)
         cr = encode(&tm_v, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(a.v), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr == CUDA_SUCCESS) {
+        const cuuint64_t qdims[3] = {(cuuint64_t)a.H * D, (cuuint64_t)a.S, (cuuint64_t)a.B};
+        const cuuint64_t qstrides[2] = {(cuuint64_t)a.H * D * 4, (cuuint64_t)a.S * a.H * D * 4};
+        const cuuint32_t qbox[3] = {(cuuint32_t)C::CH, (cuuint32_t)kPfBM, 1};
+        cr = encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(a.q), qdims, qstrides, qbox, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (cr != CUDA_SUCCESS) return set_error(RKV_ERR_LAUNCH, "attn_prefill: tensor map encode failed (%d)", (int)cr);
     auto kern = prefill_tc_kernel<D>;
     static bool attr_done[64] = {false};
@@ -561,7 +597,7 @@ static rkv_status launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream)
     const int n_qtiles = (a.S + kPfBM - 1) / kPfBM;
     const int64_t grid = (int64_t)n_qtiles * a.B * a.H;
     if (grid > 0x7FFFFFFF) return set_error(RKV_ERR_UNSUPPORTED, "attn_prefill: grid too large");
-    kern<<<(unsigned)grid, kPfThreads, C::SMEM, stream>>>(tm_k, tm_v, a.q, a.o, a.B, a.S, a.H, a.Hk, a.causal ? 1 : 0,
+    kern<<<(unsigned)grid, kPfThreads, C::SMEM, stream>>>(tm_k, tm_v, tm_q, a.o, a.B, a.S, a.H, a.Hk, a.causal ? 1 : 0,
                                                            a.seq_lens, a.scale * kPfLog2e, n_qtiles, a.flags);
     return check_launch("attn_prefill");
 }
