@@ -38,7 +38,8 @@
 namespace rkv {
 
 constexpr int kPfBM = 128;                    // query rows per CTA (TMEM lanes)
-constexpr int kPfThreads = 320;               // 10 warps
+constexpr int kPfThreads = 352;               // 11 warps
+constexpr int kPfPvWarp = 10;                 // PV issuer
 constexpr int kPfSoftmaxWarp0 = 2;
 constexpr int kPfVWarp0 = 6;
 constexpr uint32_t kPfTmemCols = 512;
@@ -55,13 +56,12 @@ struct PfCfg {
     static constexpr int TILE = BN * D * 4;                 // bytes of one K or V^T tile
     static constexpr int NK = D >= 64 ? 3 : 4;              // K stages
     static constexpr int NV = D >= 64 ? 3 : 4;              // V^T stages
-    // The tensor core needs ~100 cycles per MMA that accumulates into the result of the
-    // previous one, so long K chains are latency-bound.  D = 128: QK^T is split over the
-    // two halves of D into two accumulators (S = S_a + S_b).  D <= 64: PV is split over
+    // S/P buffers in TMEM: the MMA issuer runs up to NSBUF blocks of QK^T ahead of the
+    // softmax, so the tensor core always has queued work.  D <= 64: PV is split over
     // even/odd key steps into two accumulators (O = O_a + O_b).
-    static constexpr int QK_SPLIT = D == 128 ? 2 : 1;
+    static constexpr int NSBUF = D == 128 ? 4 : 2;
     static constexpr int PV_SPLIT = D <= 64 ? 2 : 1;
-    static constexpr int S_BUF = BN * QK_SPLIT;            // TMEM columns of one S buffer
+    static constexpr int S_BUF = BN;                       // TMEM columns of one S buffer
     static constexpr uint32_t K_SWIZZLE = D >= 32 ? kSwizzle128B : kSwizzle64B;
     // Q arrives by TMA into V ring slots 1 .. QSLOTS (free until V blocks 1.. are loaded)
     static constexpr int QSLOTS = kPfBM / BN;
@@ -71,22 +71,23 @@ struct PfCfg {
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + NK * TILE;
     static constexpr int OFF_BAR = OFF_V + NV * TILE;
-    // barriers: k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], v_loaded[NV], s_full[2],
-    //           p_ready[2], o_done, o_final, q_ready, drain, q_loaded
-    static constexpr int NBAR = 2 * NK + 3 * NV + 2 + 2 + 5;
+    // barriers: k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], v_loaded[NV], s_full[NSBUF],
+    //           p_ready[NSBUF], o_done[NSBUF], o_final, q_ready, drain, q_loaded, drain_pv
+    static constexpr int NBAR = 2 * NK + 3 * NV + 3 * NSBUF + 5;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;     // tmem base, abort flag
     static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM = (SMEM_USED + 1024 > kPfMinSmem ? SMEM_USED + 1024 : kPfMinSmem);
     static_assert(SMEM <= 227 * 1024, "prefill shared memory budget");
-    static_assert(kColS + 2 * S_BUF <= (int)kPfTmemCols && kColO + PV_SPLIT * D <= kColS && D <= 128,
+    static_assert(kColS + NSBUF * S_BUF <= (int)kPfTmemCols && kColO + PV_SPLIT * D <= kColS && D <= 128,
                   "TMEM budget");
 };
 
 struct PfBars {
-    uint32_t k_full, k_empty, v_full, v_empty, v_loaded, s_full, p_ready, o_done, o_final, q_ready, drain, q_loaded;
+    uint32_t k_full, k_empty, v_full, v_empty, v_loaded, s_full, p_ready, o_done, o_final, q_ready, drain, q_loaded,
+        drain_pv;
 };
 
-template <int NK, int NV>
+template <int NK, int NV, int NSB>
 __device__ __forceinline__ PfBars pf_bars(uint32_t base) {
     PfBars b;
     b.k_full = base;
@@ -95,12 +96,13 @@ __device__ __forceinline__ PfBars pf_bars(uint32_t base) {
     b.v_empty = b.v_full + 8 * NV;
     b.v_loaded = b.v_empty + 8 * NV;
     b.s_full = b.v_loaded + 8 * NV;
-    b.p_ready = b.s_full + 16;
-    b.o_done = b.p_ready + 16;
-    b.o_final = b.o_done + 8;
+    b.p_ready = b.s_full + 8 * NSB;
+    b.o_done = b.p_ready + 8 * NSB;
+    b.o_final = b.o_done + 8 * NSB;
     b.q_ready = b.o_final + 8;
     b.drain = b.q_ready + 8;
     b.q_loaded = b.drain + 8;
+    b.drain_pv = b.q_loaded + 8;
     return b;
 }
 
@@ -115,7 +117,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
-    const PfBars bar = pf_bars<C::NK, C::NV>(smem_addr(smem + C::OFF_BAR));
+    const PfBars bar = pf_bars<C::NK, C::NV, C::NSBUF>(smem_addr(smem + C::OFF_BAR));
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -152,15 +154,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             mbar_init(bar.v_empty + 8 * s, 1);
             mbar_init(bar.v_loaded + 8 * s, 1);
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < C::NSBUF; ++s) {
             mbar_init(bar.s_full + 8 * s, 1);
             mbar_init(bar.p_ready + 8 * s, 128);
+            mbar_init(bar.o_done + 8 * s, 1);
         }
-        mbar_init(bar.o_done, 1);
         mbar_init(bar.o_final, 1);
         mbar_init(bar.q_ready, 128);
         mbar_init(bar.drain, 1);
         mbar_init(bar.q_loaded, 1);
+        mbar_init(bar.drain_pv, 1);
         *abort_flag = 0;
         fence_barrier_init();
         prefetch_tmap(&tm_k);
@@ -212,72 +215,84 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     if (q_issued) mbar_drain(bar.q_loaded, 0, 100000000ull);
                 }
             }
-        } else if (warp == 1) {
-            // ============================================================ MMA issuer
+        } else if (warp == 1 || warp == kPfPvWarp) {
+            // ============================================================ MMA issuers
+            // Two threads issue: warp 1 the QK^T MMAs, warp 10 the PV MMAs.  A thread needs
+            // ~45 cycles per tcgen05.mma it issues, more than one N=64 MMA takes to run,
+            // so a single issuer would starve the tensor core.
             if (lane == 0) {
+                const bool qk_role = warp == 1;
                 constexpr uint32_t id_qk = idesc_tf32(kPfBM, BN, false);
                 constexpr uint32_t id_pv = idesc_tf32(kPfBM, D, false);
-                bool ok = mbar_wait(bar.q_ready, 0, abort_flag, flags);
+                bool ok = true;
                 int issued_any = 0;
                 // Descriptors are built once per ring stage; a k step only adds its byte
                 // offset (>> 4) to the start-address field, which cannot carry out of it
-                // (shared addresses are below 2^18).  Keeping the issue loop lean matters:
-                // one thread must issue an MMA every ~32-64 cycles to keep the tensor core fed.
+                // (shared addresses are below 2^18).
                 const uint64_t kdesc0 = smem_desc(smem_addr(smem + C::OFF_K), 16, C::K_ATOM, C::K_SWIZZLE);
                 const uint64_t vdesc0 = smem_desc(smem_addr(smem + C::OFF_V), 16, 1024, kSwizzle128B);
-                auto issue_qk = [&](int j) -> bool {
-                    const int s = j % C::NK;
-                    if (!mbar_wait(bar.k_full + 8 * s, (uint32_t)(j / C::NK) & 1u, abort_flag, flags)) return false;
-                    tc_fence_after();
-                    const uint64_t kd = kdesc0 + (uint64_t)(s * (C::TILE >> 4));
-                    const uint32_t d_tmem = tmem + kColS + (uint32_t)((j & 1) * C::S_BUF);
-                    constexpr int KSTEPS = D / 8 / C::QK_SPLIT;     // steps per accumulator chain
+                if (qk_role) {
+                    ok = mbar_wait(bar.q_ready, 0, abort_flag, flags);
+                    // S_j goes to buffer j % NSBUF; before QK_j overwrites the buffer of block
+                    // j - NSBUF, PV_{j-NSBUF} must have finished reading P from it.  The wait
+                    // is exact: PV_{j-2*NSBUF} completed before QK_{j-NSBUF} was issued, and
+                    // PV_j cannot have started (it needs S_j).
+                    for (int j = 0; ok && j < nblk; ++j) {
+                        const int sb = j % C::NSBUF;
+                        if (j >= C::NSBUF &&
+                            !(ok = mbar_wait(bar.o_done + 8 * sb, (uint32_t)((j - C::NSBUF) / C::NSBUF) & 1u,
+                                             abort_flag, flags)))
+                            break;
+                        const int s = j % C::NK;
+                        if (!(ok = mbar_wait(bar.k_full + 8 * s, (uint32_t)(j / C::NK) & 1u, abort_flag, flags))) break;
+                        tc_fence_after();
+                        const uint64_t kd = kdesc0 + (uint64_t)(s * (C::TILE >> 4));
+                        const uint32_t d_tmem = tmem + kColS + (uint32_t)(sb * C::S_BUF);
 #pragma unroll
-                    for (int ks = 0; ks < KSTEPS; ++ks) {
-#pragma unroll
-                        for (int part = 0; part < C::QK_SPLIT; ++part) {   // interleave the chains
-                            const int k = part * KSTEPS + ks;
+                        for (int k = 0; k < D / 8; ++k) {
                             const int c = k / (C::CH / 8), kk = k % (C::CH / 8);
                             const uint64_t bdesc = kd + (uint64_t)((c * BN * C::CH * 4 + kk * 32) >> 4);
-                            mma_tf32_ts(d_tmem + part * BN, tmem + kColQ + 8 * k, bdesc, id_qk, ks > 0 ? 1u : 0u);
+                            mma_tf32_ts(d_tmem, tmem + kColQ + 8 * k, bdesc, id_qk, k > 0 ? 1u : 0u);
                         }
+                        mma_commit(bar.s_full + 8 * sb);
+                        mma_commit(bar.k_empty + 8 * s);
+                        issued_any = 1;
                     }
-                    mma_commit(bar.s_full + 8 * (j & 1));
-                    mma_commit(bar.k_empty + 8 * s);
-                    issued_any = 1;
-                    return true;
-                };
-                if (ok) ok = issue_qk(0);
-                for (int j = 1; ok && j <= nblk; ++j) {
-                    if (j < nblk && !(ok = issue_qk(j))) break;
-                    // O += P_{j-1} V_{j-1}
-                    const int pj = j - 1;
-                    const int sv = pj % C::NV;
-                    if (!(ok = mbar_wait(bar.p_ready + 8 * (pj & 1), (uint32_t)(pj >> 1) & 1u, abort_flag, flags))) break;
-                    if (!(ok = mbar_wait(bar.v_full + 8 * sv, (uint32_t)(pj / C::NV) & 1u, abort_flag, flags))) break;
-                    tc_fence_after();
-                    const uint64_t vd = vdesc0 + (uint64_t)(sv * (C::TILE >> 4));
-                    const uint32_t a_tmem = tmem + kColS + (uint32_t)((pj & 1) * C::S_BUF);
-                    const uint32_t first = pj > 0 ? 1u : 0u;
+                    if (!ok && issued_any) {   // unwinding: let issued MMAs finish before TMEM is freed
+                        mma_commit(bar.drain);
+                        mbar_drain(bar.drain, 0, 100000000ull);
+                    }
+                } else {
+                    for (int pj = 0; ok && pj < nblk; ++pj) {
+                        // O += P_pj V_pj
+                        const int sv = pj % C::NV, sb = pj % C::NSBUF;
+                        if (!(ok = mbar_wait(bar.p_ready + 8 * sb, (uint32_t)(pj / C::NSBUF) & 1u, abort_flag, flags))) break;
+                        if (!(ok = mbar_wait(bar.v_full + 8 * sv, (uint32_t)(pj / C::NV) & 1u, abort_flag, flags))) break;
+                        tc_fence_after();
+                        const uint64_t vd = vdesc0 + (uint64_t)(sv * (C::TILE >> 4));
+                        const uint32_t a_tmem = tmem + kColS + (uint32_t)(sb * C::S_BUF);
+                        const uint32_t first = pj > 0 ? 1u : 0u;
 #pragma unroll
-                    for (int k = 0; k < BN / 8; ++k) {
-                        // V^T tile: rows = d, 32 keys per 128-byte row, key chunks D*128 bytes apart
-                        const uint64_t bdesc = vd + (uint64_t)(((k / 4) * (D * 128) + (k % 4) * 32) >> 4);
-                        const int part = k % C::PV_SPLIT;
-                        mma_tf32_ts(tmem + kColO + part * D, a_tmem + 8 * k, bdesc, id_pv,
-                                    k >= C::PV_SPLIT ? 1u : first);
+                        for (int k = 0; k < BN / 8; ++k) {
+                            // V^T tile: rows = d, 32 keys per 128-byte row, key chunks D*128 bytes apart
+                            const uint64_t bdesc = vd + (uint64_t)(((k / 4) * (D * 128) + (k % 4) * 32) >> 4);
+                            const int part = k % C::PV_SPLIT;
+                            mma_tf32_ts(tmem + kColO + part * D, a_tmem + 8 * k, bdesc, id_pv,
+                                        k >= C::PV_SPLIT ? 1u : first);
+                        }
+                        mma_commit(bar.o_done + 8 * sb);
+                        mma_commit(bar.v_empty + 8 * sv);
+                        issued_any = 1;
                     }
-                    mma_commit(bar.o_done);
-                    mma_commit(bar.v_empty + 8 * sv);
-                }
-                if (ok) {
-                    mma_commit(bar.o_final);
-                } else if (issued_any) {   // unwinding: let issued MMAs finish before TMEM is freed
-                    mma_commit(bar.drain);
-                    mbar_drain(bar.drain, 0, 100000000ull);
+                    if (ok) {
+                        mma_commit(bar.o_final);
+                    } else if (issued_any) {
+                        mma_commit(bar.drain_pv);
+                        mbar_drain(bar.drain_pv, 0, 100000000ull);
+                    }
                 }
             }
-        } else if (warp >= kPfVWarp0) {
+        } else if (warp >= kPfVWarp0 && warp < kPfVWarp0 + 4) {
             // ============================================================ V transposer
             // V tiles arrive by TMA in the same swizzled layout as K (rows = keys).  The
             // transposer rewrites each slot in place as V^T: work item = (key quad aa,
@@ -395,26 +410,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             bool ok = true;
             const int key_lim = causal ? min(qi + 1, len) : len;   // keys visible to this row
             for (int j = 0; j < nblk; ++j) {
-                ok = mbar_wait(bar.s_full + 8 * (j & 1), (uint32_t)(j >> 1) & 1u, abort_flag, flags);
+                ok = mbar_wait(bar.s_full + 8 * (j % C::NSBUF), (uint32_t)(j / C::NSBUF) & 1u, abort_flag, flags);
                 if (!(ok = __all_sync(0xffffffffu, ok))) break;   // warp-uniform before TMEM access
                 tc_fence_after();
-                const uint32_t s_col = lane_base + kColS + (uint32_t)((j & 1) * C::S_BUF);
+                const uint32_t s_col = lane_base + kColS + (uint32_t)((j % C::NSBUF) * C::S_BUF);
                 float s[BN];
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t w[32];
                     tmem_ld32(s_col + 32 * c, w);
-                    if constexpr (C::QK_SPLIT == 2) {
-                        uint32_t w2[32];
-                        tmem_ld32(s_col + BN + 32 * c, w2);
-                        tmem_wait_ld();
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(w[e]) + __uint_as_float(w2[e]);
-                    } else {
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(w[e]);
-                    }
+                    for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(w[e]);
                 }
                 const int k0 = j * BN;
                 const int nvis = min(max(key_lim - k0, 0), BN);     // visible keys of this block
@@ -453,8 +460,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 m_run = m_use;
                 tmem_wait_st();
                 if (j > 0 && __any_sync(0xffffffffu, need)) {
-                    // O holds blocks < j once PV_{j-1} completes; scale it by alpha
-                    ok = mbar_wait(bar.o_done, (uint32_t)(j - 1) & 1u, abort_flag, flags);
+                    // O holds blocks < j once PV_{j-1} completes; scale it by alpha.  Seeing S_j
+                    // means PV_{j-NSBUF} completed (issued before QK_j), so the barrier of
+                    // PV_{j-1}'s buffer is at most one phase behind: the parity wait is exact.
+                    ok = mbar_wait(bar.o_done + 8 * ((j - 1) % C::NSBUF), (uint32_t)((j - 1) / C::NSBUF) & 1u,
+                                   abort_flag, flags);
                     if (!(ok = __all_sync(0xffffffffu, ok))) break;
                     tc_fence_after();
 #pragma unroll
@@ -478,7 +488,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     tmem_wait_st();
                 }
                 tc_fence_before();
-                mbar_arrive(bar.p_ready + 8 * (j & 1));
+                mbar_arrive(bar.p_ready + 8 * (j % C::NSBUF));
             }
             // ---------------------------------------------------------- epilogue
             if (ok) ok = mbar_wait(bar.o_final, 0, abort_flag, flags);
