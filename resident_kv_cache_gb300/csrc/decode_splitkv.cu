@@ -13,9 +13,9 @@
 //  * One persistent CTA per SM takes an equal contiguous share of the R rows
 //    (balanced to one row whatever the length mix); the share may cross
 //    segment boundaries, and each part of a segment in one CTA is a "piece".
-//  * A producer warp streams 64-row tiles of K and V with bulk async copies
-//    into a 3-stage shared-memory ring (mbarrier full/empty pairs).
-//  * Eight consumer warps each take 8 rows of a tile.  GQA: the G = H/Hk query
+//  * A producer warp streams tiles of K and V (8 rows per consumer warp) with bulk
+//    async copies into a 2-4 stage shared-memory ring (mbarrier full/empty pairs).
+//  * Twelve consumer warps (eight for G = 8) each take 8 rows of a tile.  GQA: the G = H/Hk query
 //    heads that share a kv head are processed together, so every cache row is
 //    read from HBM once per kv head.  Dot products are split over D/4 lanes and
 //    reduced with a transposing butterfly (one shuffle per partial, not one per
@@ -29,11 +29,7 @@
 
 namespace rkv {
 
-constexpr int kDecConsumerWarps = 8;
-constexpr int kDecThreads = (kDecConsumerWarps + 1) * 32;
-constexpr int kDecConsumerThreads = kDecConsumerWarps * 32;
 constexpr int kDecBatchRows = 8;                                   // rows per warp per tile
-constexpr int kDecTileRows = kDecBatchRows * kDecConsumerWarps;    // 64
 constexpr int kDecMaxCtas = 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -41,6 +37,12 @@ __host__ __device__ constexpr int ilog2c(int x) { return x <= 1 ? 0 : 1 + ilog2c
 
 template <int D, int G>
 struct DecCfg {
+    // Consumer warps: 12 (four per SM sub-partition, <= 128 registers each) hide the
+    // shared-memory and shuffle latencies better than 8; G = 8 needs more registers.
+    static constexpr int W = G <= 4 ? 12 : 8;
+    static constexpr int CT = W * 32;                 // consumer threads
+    static constexpr int THREADS = CT + 32;           // + one producer warp
+    static constexpr int TILE_ROWS = kDecBatchRows * W;
     static constexpr int LPR = D / 4;                 // lanes per cache row (one float4 each)
     static constexpr int RPW = 32 / LPR;              // rows a warp covers per pass
     static constexpr int PASSES = kDecBatchRows / RPW;
@@ -48,15 +50,18 @@ struct DecCfg {
     static constexpr int NVR = NV >= LPR ? NV / LPR : 1;   // totals per lane after the butterfly
     static constexpr int ENTRIES = kDecBatchRows * G; // scores per warp per tile
     static constexpr int EPL = ENTRIES >= 32 ? ENTRIES / 32 : 1;
-    static constexpr int NST = (D == 128) ? (G == 8 ? 2 : 3) : 4;  // pipeline stages
     static constexpr int REC = ((G * D + 2 * G) + 3) / 4 * 4;      // floats per partial record
-    // shared memory layout (bytes)
-    static constexpr int TILE_BYTES = kDecTileRows * D * 4;
+    // shared memory layout (bytes): as many K/V stages as fit beside the reduction buffers
+    static constexpr int TILE_BYTES = TILE_ROWS * D * 4;
+    static constexpr int SIDE = W * ENTRIES * 4 + W * G * D * 4 + W * 2 * G * 4 + 34 * 8 + 32 * 4 + 2 * 4 * 8 + 16;
+    static constexpr int NST_FIT = (226 * 1024 - SIDE) / (2 * TILE_BYTES);
+    static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;          // pipeline stages
+    static_assert(NST >= 2, "decode pipeline needs two stages");
     static constexpr int OFF_STAGES = 0;
     static constexpr int OFF_SC = OFF_STAGES + NST * 2 * TILE_BYTES;
-    static constexpr int OFF_RED_ACC = OFF_SC + kDecConsumerWarps * ENTRIES * 4;
-    static constexpr int OFF_RED_ML = OFF_RED_ACC + kDecConsumerWarps * G * D * 4;
-    static constexpr int OFF_P = OFF_RED_ML + kDecConsumerWarps * 2 * G * 4;      // int64 P[33]
+    static constexpr int OFF_RED_ACC = OFF_SC + W * ENTRIES * 4;
+    static constexpr int OFF_RED_ML = OFF_RED_ACC + W * G * D * 4;
+    static constexpr int OFF_P = OFF_RED_ML + W * 2 * G * 4;      // int64 P[33]
     static constexpr int OFF_L = OFF_P + 34 * 8;                                  // int L[32]
     static constexpr int OFF_BAR = OFF_L + 32 * 4;                                // full/empty
     static constexpr int OFF_MISC = OFF_BAR + 2 * NST * 8;                        // abort, last
@@ -114,7 +119,7 @@ __device__ __forceinline__ void locate(int64_t pos, const int64_t* P, const int*
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kDecThreads, 1)
+__global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1)
 decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_cache,
                       const float* __restrict__ v_cache, float* __restrict__ out, int M, int Hk, int Lmax,
                       const int* __restrict__ seq_lens, float scale_log2, int* __restrict__ tickets,
@@ -157,7 +162,7 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
     if (threadIdx.x == 32) {
         for (int s = 0; s < C::NST; ++s) {
             mbar_init(smem_addr(&bars[s]), 1);                          // full: producer arrival + tx
-            mbar_init(smem_addr(&bars[C::NST + s]), kDecConsumerWarps);  // empty: one per consumer warp
+            mbar_init(smem_addr(&bars[C::NST + s]), C::W);  // empty: one per consumer warp
         }
         fence_barrier_init();
     }
@@ -166,7 +171,7 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
     const int64_t R = P[M];
     const int64_t r0 = share_begin(c, R, n), r1 = share_begin(c + 1, R, n);
 
-    if (warp == kDecConsumerWarps) {
+    if (warp == C::W) {
         // ================================================================ producer
         if (lane == 0) {
             int issued[C::NST > 0 ? C::NST : 1];
@@ -180,11 +185,11 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
                 locate(pos, P, L, Hk, m, kh, seg_start);
                 const int64_t piece_end = min(r1, seg_start + L[m]);
                 const int64_t head_row0 = ((int64_t)m * Hk + kh) * Lmax - seg_start;  // flat -> cache row
-                for (int64_t t0 = pos; t0 < piece_end; t0 += kDecTileRows, ++it) {
+                for (int64_t t0 = pos; t0 < piece_end; t0 += C::TILE_ROWS, ++it) {
                     const int s = it % C::NST;
                     const uint32_t ph = (uint32_t)(it / C::NST) & 1u;
                     if (!mbar_wait(smem_addr(&bars[C::NST + s]), ph ^ 1u, abort_flag, flags)) { ok = false; break; }
-                    const int rows = (int)min((int64_t)kDecTileRows, piece_end - t0);
+                    const int rows = (int)min((int64_t)C::TILE_ROWS, piece_end - t0);
                     const uint32_t bytes = (uint32_t)rows * D * 4;
                     const uint32_t full = smem_addr(&bars[s]);
                     mbar_arrive_expect_tx(full, 2 * bytes);
@@ -209,7 +214,7 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
     for (int sg = c; sg < M * Hk; sg += n) {
         const int m = sg / Hk, kh = sg % Hk;
         if (L[m] == 0)
-            for (int i = threadIdx.x; i < G * D; i += kDecConsumerThreads)
+            for (int i = threadIdx.x; i < G * D; i += C::CT)
                 out[(int64_t)m * H * D + (int64_t)(kh * G) * D + i] = 0.0f;
     }
 
@@ -240,11 +245,11 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
         m_run = -INFINITY;
         l_run = 0.0f;
 
-        for (int64_t t0 = pos; t0 < piece_end; t0 += kDecTileRows, ++it) {
+        for (int64_t t0 = pos; t0 < piece_end; t0 += C::TILE_ROWS, ++it) {
             const int s = it % C::NST;
             const uint32_t ph = (uint32_t)(it / C::NST) & 1u;
             if (ok) ok = mbar_wait(smem_addr(&bars[s]), ph, abort_flag, flags);
-            const int tile_rows = (int)min((int64_t)kDecTileRows, piece_end - t0);
+            const int tile_rows = (int)min((int64_t)C::TILE_ROWS, piece_end - t0);
             const int nvalid = min(max(tile_rows - warp * kDecBatchRows, 0), kDecBatchRows);
             if (ok && nvalid > 0) {
                 const float4* Ks = reinterpret_cast<const float4*>(smem + C::OFF_STAGES + (2 * s) * C::TILE_BYTES) +
@@ -354,7 +359,7 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
             red_ml[(warp * G + lane) * 2 + 0] = m_run;
             red_ml[(warp * G + lane) * 2 + 1] = l_run;
         }
-        named_barrier(1, kDecConsumerThreads);
+        named_barrier(1, C::CT);
 
         const int sg = m * Hk + kh;
         const int c_first = owner_of(seg_start, R, n);
@@ -362,15 +367,15 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
         const bool single = (c_first == c_last);
         float* my_rec = records + (int64_t)(sg + c) * C::REC;
         float* o_seg = out + (int64_t)m * H * D + (int64_t)(kh * G) * D;
-        for (int i = threadIdx.x; i < G * D; i += kDecConsumerThreads) {
+        for (int i = threadIdx.x; i < G * D; i += C::CT) {
             const int h = i / D, d = i % D;
             float mx = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < kDecConsumerWarps; ++w) mx = fmaxf(mx, red_ml[(w * G + h) * 2]);
+            for (int w = 0; w < C::W; ++w) mx = fmaxf(mx, red_ml[(w * G + h) * 2]);
             float l = 0.0f, o = 0.0f;
             if (mx != -INFINITY) {
 #pragma unroll
-                for (int w = 0; w < kDecConsumerWarps; ++w) {
+                for (int w = 0; w < C::W; ++w) {
                     const float mw = red_ml[(w * G + h) * 2];
                     const float f = (mw == -INFINITY) ? 0.0f : fast_exp2(mw - mx);
                     l += red_ml[(w * G + h) * 2 + 1] * f;
@@ -389,7 +394,7 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
         }
         if (!single) {
             __threadfence();
-            named_barrier(1, kDecConsumerThreads);
+            named_barrier(1, C::CT);
             if (threadIdx.x == 0) {
                 // pieces = CTAs in [c_first, c_last] that own rows (a share is empty only when R < n)
                 int pieces = 0;
@@ -399,10 +404,10 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
                 if (ok) last = (atomicAdd(tickets + sg, 1) == pieces - 1);
                 *last_flag = last;
             }
-            named_barrier(1, kDecConsumerThreads);
+            named_barrier(1, C::CT);
             if (*last_flag) {
                 __threadfence();
-                for (int i = threadIdx.x; i < G * D; i += kDecConsumerThreads) {
+                for (int i = threadIdx.x; i < G * D; i += C::CT) {
                     const int h = i / D;
                     float mx = -INFINITY;
                     for (int cc = c_first; cc <= c_last; ++cc)
@@ -424,7 +429,7 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
                 if (threadIdx.x == 0) tickets[sg] = 0;
             }
         }
-        named_barrier(1, kDecConsumerThreads);   // red_* free for the next piece
+        named_barrier(1, C::CT);   // red_* free for the next piece
         pos = piece_end;
     }
 }
@@ -464,7 +469,7 @@ static rkv_status launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
     if (n > kDecMaxCtas) n = kDecMaxCtas;
     int* tickets = static_cast<int*>(a.workspace);
     float* records = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + tickets_bytes(a.M, a.Hk));
-    kern<<<n, kDecThreads, C::SMEM, stream>>>(a.q, a.k_cache, a.v_cache, a.o, a.M, a.Hk, a.Lmax, a.seq_lens,
+    kern<<<n, C::THREADS, C::SMEM, stream>>>(a.q, a.k_cache, a.v_cache, a.o, a.M, a.Hk, a.Lmax, a.seq_lens,
                                                a.scale * kLog2e, tickets, records, a.flags);
     return check_launch("attn_decode_batched");
 }
