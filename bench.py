@@ -48,8 +48,8 @@ WORKLOAD = ("causal GQA prefill B=4 S=2048 H=32 Hk=8 D=128 + cache fill into [4,
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50)
-    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["rkv", "reference"], default="rkv")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -126,7 +126,7 @@ def kernel_hash(*files):
     return h.hexdigest()[:16]
 
 
-KERNEL_FILES = {"prefill": ("prefill_simt.cu",), "decode": ("decode_splitkv.cu",), "scatter": ("kv_scatter.cu",)}
+KERNEL_FILES = {"prefill": ("prefill_tc.cu",), "decode": ("decode_splitkv.cu",), "scatter": ("kv_scatter.cu",)}
 
 
 def ncu_traffic(kernel):
@@ -342,34 +342,38 @@ def run_e2e(W, torch, rkv, stream, K):
             "note": "decode KV cache stays resident; per-step inputs and outputs cross PCIe/C2C"}
 
 
-def cpu_baseline(host_decode, host_prefill, budget_s=20.0):
-    """The oracle (test infrastructure) timed on this host's cores on a bounded sample."""
+def cpu_baseline(host_decode, host_prefill, decode_budget_s=10.0, prefill_budget_s=5.0):
+    """The oracle (test infrastructure) timed on this host's cores on a bounded sample:
+    whole batched decode steps repeated for ~10 s, then random causal prefill rows for ~5 s."""
     import oracle
     oracle.build()
     x = host_decode
     Dd, P = DECODE, PREFILL
-    # decode: whole batched decode step (all 32 sequences)
     hk, hv = x["k_cache"].copy(), x["v_cache"].copy()
-    t0 = time.perf_counter()
-    oracle.scatter(x["k_new"], x["v_new"], hk, hv, Dd.M, 1, Dd.Hk, Dd.D, Dd.Lmax, x["start_pos"],
-                   inplace=True)
-    t1 = time.perf_counter()
-    oracle.decode(x["q"], hk, hv, Dd.M, Dd.H, Dd.Hk, Dd.D, Dd.Lmax, x["lens"])
-    t2 = time.perf_counter()
     kv_bytes, _ = decode_bytes(x["lens"])
-    dec_gbs = kv_bytes / (t2 - t1) / 1e9
-    # prefill: a sample of query rows, scaled by the FLOPs those rows carry
+    reps, t_dec = 0, 0.0
+    while t_dec < decode_budget_s and reps < 10000:
+        t0 = time.perf_counter()
+        oracle.scatter(x["k_new"], x["v_new"], hk, hv, Dd.M, 1, Dd.Hk, Dd.D, Dd.Lmax, x["start_pos"],
+                       inplace=True)
+        oracle.decode(x["q"], hk, hv, Dd.M, Dd.H, Dd.Hk, Dd.D, Dd.Lmax, x["lens"])
+        t_dec += time.perf_counter() - t0
+        reps += 1
     q, k, v = host_prefill
-    n_rows = 512
-    rows = inputs.sample_indices(P.B * P.H * P.S, n_rows, 5)
-    t3 = time.perf_counter()
-    oracle.prefill_rows(q, k, v, P.B, P.S, P.H, P.Hk, P.D, True, rows)
-    t4 = time.perf_counter()
-    flops = float(np.sum(4.0 * P.D * ((rows % P.S) + 1)))
-    return {"value": dec_gbs, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": "one whole batched decode step (32 sequences) for GB/s; 512 random causal prefill "
-                      "rows for TFLOP/s", "prefill_tflops": flops / (t4 - t3) / 1e12,
-            "seconds": round(t4 - t0, 2), "scatter_s": round(t1 - t0, 3)}
+    rows_done, flops, t_pre, chunk = 0, 0.0, 0.0, 0
+    while t_pre < prefill_budget_s and chunk < 1000:
+        rows = inputs.sample_indices(P.B * P.H * P.S, 1024, 100 + chunk)
+        t0 = time.perf_counter()
+        oracle.prefill_rows(q, k, v, P.B, P.S, P.H, P.Hk, P.D, True, rows)
+        t_pre += time.perf_counter() - t0
+        flops += float(np.sum(4.0 * P.D * ((rows % P.S) + 1)))
+        rows_done += rows.size
+        chunk += 1
+    return {"value": kv_bytes * reps / t_dec / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{reps} whole batched decode steps (scatter + decode of 32 sequences) in "
+                      f"{t_dec:.1f} s for GB/s; {rows_done} random causal prefill rows in {t_pre:.1f} s "
+                      "for TFLOP/s", "prefill_tflops": flops / t_pre / 1e12}
 
 
 def run_reference(args):
