@@ -54,7 +54,10 @@ struct PfCfg {
     static constexpr int CH = D >= 32 ? 32 : D;             // floats per swizzled K row chunk
     static constexpr int NCH = D / CH;
     static constexpr int TILE = BN * D * 4;                 // bytes of one K or V^T tile
-    static constexpr int NK = D >= 64 ? 3 : 4;              // K stages
+    // D = 128: K slots come in adjacent pairs so one N = 128 MMA chain computes the scores
+    // of two 64-key blocks (half the MMAs of N = 64; a thread needs ~45+ cycles per issue).
+    static constexpr bool KPAIR = D == 128;
+    static constexpr int NK = KPAIR ? 4 : (D >= 64 ? 3 : 4);   // K stages
     static constexpr int NV = D >= 64 ? 3 : 4;              // V^T stages
     // S/P buffers in TMEM: the MMA issuer runs up to NSBUF blocks of QK^T ahead of the
     // softmax, so the tensor core always has queued work.  D <= 64: PV is split over
@@ -69,6 +72,12 @@ struct PfCfg {
     static constexpr uint32_t K_ATOM = D >= 32 ? 1024 : 512; // 8 rows x swizzle span
     // shared memory layout (offsets from a 1024-aligned base)
     static constexpr int OFF_K = 0;
+    // byte offset of d-chunk c of K slot s: paired slots interleave their chunks so the
+    // 2*BN rows of a chunk are contiguous (uniform 1024-byte stride per 8 rows)
+    __host__ __device__ static constexpr int koff(int s, int c) {
+        return KPAIR ? (s / 2) * 2 * TILE + c * (2 * BN * CH * 4) + (s % 2) * (BN * CH * 4)
+                     : s * TILE + c * (BN * CH * 4);
+    }
     static constexpr int OFF_V = OFF_K + NK * TILE;
     static constexpr int OFF_BAR = OFF_V + NV * TILE;
     // barriers: k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], v_loaded[NV], s_full[NSBUF],
@@ -203,10 +212,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag, flags)) break;
                     const uint32_t full = full0 + 8 * s;
                     mbar_arrive_expect_tx(full, C::TILE);
-                    const uint32_t dst = smem_addr(smem + off0 + s * C::TILE);
+                    const uint32_t dst = smem_addr(smem + off0);
 #pragma unroll
                     for (int c = 0; c < C::NCH; ++c)
-                        tma_load_3d(dst + c * BN * C::CH * 4, tm, g * D + c * C::CH, j * BN, b, full);
+                        tma_load_3d(dst + (is_k ? C::koff(s, c) : s * C::TILE + c * BN * C::CH * 4), tm,
+                                    g * D + c * C::CH, j * BN, b, full);
                     issued = j + 1;
                 }
                 if (*abort_flag) {   // unwinding: let issued copies land
@@ -233,29 +243,35 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const uint64_t vdesc0 = smem_desc(smem_addr(smem + C::OFF_V), 16, 1024, kSwizzle128B);
                 if (qk_role) {
                     ok = mbar_wait(bar.q_ready, 0, abort_flag, flags);
-                    // S_j goes to buffer j % NSBUF; before QK_j overwrites the buffer of block
-                    // j - NSBUF, PV_{j-NSBUF} must have finished reading P from it.  The wait
-                    // is exact: PV_{j-2*NSBUF} completed before QK_{j-NSBUF} was issued, and
-                    // PV_j cannot have started (it needs S_j).
-                    for (int j = 0; ok && j < nblk; ++j) {
-                        const int sb = j % C::NSBUF;
-                        if (j >= C::NSBUF &&
-                            !(ok = mbar_wait(bar.o_done + 8 * sb, (uint32_t)((j - C::NSBUF) / C::NSBUF) & 1u,
-                                             abort_flag, flags)))
-                            break;
-                        const int s = j % C::NK;
-                        if (!(ok = mbar_wait(bar.k_full + 8 * s, (uint32_t)(j / C::NK) & 1u, abort_flag, flags))) break;
+                    // S_j goes to buffer j % NSBUF (paired blocks: two adjacent buffers); before
+                    // QK_j overwrites the buffer of block j - NSBUF, PV_{j-NSBUF} must have
+                    // finished reading P from it.  The wait is exact: PV_{j-2*NSBUF} completed
+                    // before QK_{j-NSBUF} was issued, and PV_j cannot have started (it needs S_j).
+                    constexpr uint32_t id_qk2 = idesc_tf32(kPfBM, 2 * BN, false);
+                    for (int j = 0; ok && j < nblk; j += C::KPAIR ? 2 : 1) {
+                        const int nb = (C::KPAIR && j + 1 < nblk) ? 2 : 1;   // blocks in this chain
+                        for (int bb = j; ok && bb < j + nb; ++bb) {
+                            if (bb >= C::NSBUF)
+                                ok = mbar_wait(bar.o_done + 8 * (bb % C::NSBUF),
+                                               (uint32_t)((bb - C::NSBUF) / C::NSBUF) & 1u, abort_flag, flags);
+                            if (ok)
+                                ok = mbar_wait(bar.k_full + 8 * (bb % C::NK), (uint32_t)(bb / C::NK) & 1u, abort_flag,
+                                               flags);
+                        }
+                        if (!ok) break;
                         tc_fence_after();
-                        const uint64_t kd = kdesc0 + (uint64_t)(s * (C::TILE >> 4));
-                        const uint32_t d_tmem = tmem + kColS + (uint32_t)(sb * C::S_BUF);
+                        const int s = j % C::NK;          // even when paired: slots s, s+1 share a pair
+                        const uint32_t d_tmem = tmem + kColS + (uint32_t)((j % C::NSBUF) * C::S_BUF);
 #pragma unroll
                         for (int k = 0; k < D / 8; ++k) {
                             const int c = k / (C::CH / 8), kk = k % (C::CH / 8);
-                            const uint64_t bdesc = kd + (uint64_t)((c * BN * C::CH * 4 + kk * 32) >> 4);
-                            mma_tf32_ts(d_tmem, tmem + kColQ + 8 * k, bdesc, id_qk, k > 0 ? 1u : 0u);
+                            const uint64_t bdesc = kdesc0 + (uint64_t)((C::koff(s, c) + kk * 32) >> 4);
+                            mma_tf32_ts(d_tmem, tmem + kColQ + 8 * k, bdesc, nb == 2 ? id_qk2 : id_qk, k > 0 ? 1u : 0u);
                         }
-                        mma_commit(bar.s_full + 8 * sb);
-                        mma_commit(bar.k_empty + 8 * s);
+                        for (int bb = j; bb < j + nb; ++bb) {
+                            mma_commit(bar.s_full + 8 * (bb % C::NSBUF));
+                            mma_commit(bar.k_empty + 8 * (bb % C::NK));
+                        }
                         issued_any = 1;
                     }
                     if (!ok && issued_any) {   // unwinding: let issued MMAs finish before TMEM is freed
