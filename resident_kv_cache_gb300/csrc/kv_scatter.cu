@@ -51,8 +51,8 @@ kv_scatter_kernel(const float4* __restrict__ k_new, const float4* __restrict__ v
         const float4 kv = __ldcs(k_new + src_base + idx);
         const float4 vv = __ldcs(v_new + src_base + idx);
         const int64_t dst = ((seq_base + (int64_t)kh * Lmax) + pos) * D4 + d4;
-        k_cache[dst] = kv;
-        v_cache[dst] = vv;
+        __stcs(k_cache + dst, kv);     // streaming stores: the cache is far larger than L2
+        __stcs(v_cache + dst, vv);
     }
 }
 

@@ -530,8 +530,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                         if (qi < S) {
 #pragma unroll
                             for (int e = 0; e < 8; ++e)
-                                op[c * 8 + e] = make_float4(__uint_as_float(w[4 * e]) * inv, __uint_as_float(w[4 * e + 1]) * inv,
-                                                            __uint_as_float(w[4 * e + 2]) * inv, __uint_as_float(w[4 * e + 3]) * inv);
+                                __stcs(op + c * 8 + e,     // streaming: written once, not re-read here
+                                       make_float4(__uint_as_float(w[4 * e]) * inv, __uint_as_float(w[4 * e + 1]) * inv,
+                                                   __uint_as_float(w[4 * e + 2]) * inv, __uint_as_float(w[4 * e + 3]) * inv));
                         }
                     } else {
                         uint32_t w[16], w2[16];
@@ -543,8 +544,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                         if (qi < S) {
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
-                                op[e] = make_float4(__uint_as_float(w[4 * e]) * inv, __uint_as_float(w[4 * e + 1]) * inv,
-                                                    __uint_as_float(w[4 * e + 2]) * inv, __uint_as_float(w[4 * e + 3]) * inv);
+                                __stcs(op + e, make_float4(__uint_as_float(w[4 * e]) * inv, __uint_as_float(w[4 * e + 1]) * inv,
+                                                           __uint_as_float(w[4 * e + 2]) * inv, __uint_as_float(w[4 * e + 3]) * inv));
                         }
                     }
                 }
