@@ -198,6 +198,22 @@ class Workload:
 LAUNCHES_PER_STEP = 4   # prefill, cache-fill scatter, decode-step scatter, decode
 
 
+def max_over_ranks(torch, dist, dev, values):
+    """Element-wise maximum of per-rank timings (every rank gets the result)."""
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu().tolist()]
+
+
+def decode_step_value(kv_bytes_per_rank, scatter_ms, decode_ms, world):
+    """(per-rank decode-step GB/s, whole-job GB/s).  Every rank runs the same
+    workload on its own GPU, so the job reads world x kv_bytes in the slowest
+    rank's time (the timings passed in are already the maximum over ranks)."""
+    per_rank = kv_bytes_per_rank / ((scatter_ms + decode_ms) * 1e-3) / 1e9
+    return per_rank, per_rank * world
+
+
 def run_rkv(args, rank, world, torch, dist):
     from resident_kv_cache_gb300 import binding as rkv
     from resident_kv_cache_gb300 import build as rkv_build
@@ -244,17 +260,12 @@ def run_rkv(args, rank, world, torch, dist):
     if flags & rkv.RKV_FLAG_WAIT_TIMEOUT:
         raise RuntimeError("device reported a wait timeout during the benchmark")
 
-    # max over ranks
-    vals = torch.tensor([total_ms, *part_ms.tolist()], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    total_ms, part_ms = float(vals[0]), vals[1:].cpu().numpy()
+    total_ms, *part_ms = max_over_ranks(torch, dist, dev, [total_ms, *part_ms.tolist()])
     ms_step = total_ms / K
-    prefill_ms, fill_ms, dsc_ms, dec_ms = (float(x) for x in part_ms)
+    prefill_ms, fill_ms, dsc_ms, dec_ms = part_ms
 
     kv_bytes, dec_all_bytes = decode_bytes(W.lens)
-    decode_step_gbs = kv_bytes / ((dsc_ms + dec_ms) * 1e-3) / 1e9
-    value = decode_step_gbs * world
+    decode_step_gbs, value = decode_step_value(kv_bytes, dsc_ms, dec_ms, world)
     prefill_tflops = PREFILL.flops / (prefill_ms * 1e-3) / 1e12
     peaks, peak_kind = load_peaks()
     hbm = peaks["hbm_gbs"]
