@@ -13,10 +13,13 @@
 // that alternate direction.  Rings, TMEM buffers and barrier phases run on across
 // items, so one item's prologue (Q load) and epilogue (O store) overlap the tensor-core
 // work of its neighbours.  Warp roles:
-//   warp 0       K and V producers (lanes 0 and 16): TMA (cp.async.bulk.tensor,
-//                128-byte swizzle) of BN x D tiles into NK- and NV-stage rings.
-//                The K ring carries each item's query tile ahead of its key tiles;
-//                lane 0 also prefetches the next item's query tile into L2.
+//   warp 0       K producer (one thread): TMA (cp.async.bulk.tensor, 128-byte
+//                swizzle) of BN x D tiles into an NK-stage ring that carries each
+//                item's query tile ahead of its key tiles; it also prefetches the
+//                next item's query tile into L2.
+//   warp 11      V producer (one thread): V tiles into an NV-stage ring, followed per
+//                item by output staging slots that the epilogue fills with O / l and
+//                this thread stores to the output by TMA.
 //   warp 1       QK^T issuer (one thread) and TMEM owner: per item, Q goes from
 //                the K ring into TMEM by tcgen05.cp, then per key block
 //                  S_j = Q . K_j^T   tcgen05.mma kind::tf32, A = Q from TMEM
@@ -27,7 +30,8 @@
 //                block: S row from TMEM, mask, row max, lazy rescale (O is
 //                rescaled only when the running max grows by more than 2^8),
 //                p = 2^(s*scale*log2e - m) truncated to TF32 and written back over
-//                S; per item: O / l stored to the interleaved output rows.
+//                S; per item: O / l written to the staging slots (swizzled like the
+//                TMA box, conflict-free).
 //   warps 6-9    V transposer: tcgen05 kind::tf32 reads B only K-major, so each
 //                V tile is transposed in shared memory (4x4 blocks through
 //                registers, conflict-free 16-byte stores, 128-byte swizzle).
@@ -44,9 +48,10 @@
 namespace rkv {
 
 constexpr int kPfBM = 128;                    // query rows per CTA (TMEM lanes)
-constexpr int kPfThreads = 352;               // 11 warps
+constexpr int kPfThreads = 384;               // 12 warps
 constexpr int kPfPvWarp = 10;                 // PV issuer
-constexpr int kPfVWarp0 = 6;
+constexpr int kPfVWarp0 = 6;                  // first V transposer warp
+constexpr int kPfVProdWarp = 11;              // V producer and output stores
 constexpr uint32_t kPfTmemCols = 512;
 constexpr uint32_t kColQ = 0, kColO = 128, kColS = 256;   // TMEM column bases
 constexpr float kPfLog2e = 1.4426950408889634f;
@@ -77,6 +82,11 @@ struct PfCfg {
     // aligned slot pair, so their 128 rows sit at a uniform stride like an MMA operand.
     static constexpr int QSLOTS = kPfBM / BN;
     static_assert(QSLOTS <= NK && (!KPAIR || QSLOTS == 2), "query fills in the K ring");
+    // Each item's output tile (kPfBM x D) is staged in OSLOTS V-ring slots, each holding
+    // OCH column chunks of CH floats for all kPfBM rows (swizzled like the TMA box).
+    static constexpr int OSLOTS = kPfBM / BN;
+    static constexpr int OCH = NCH / OSLOTS;
+    static_assert(OSLOTS < NV && OSLOTS * OCH == NCH && OCH * kPfBM * CH * 4 == TILE, "output staging");
     // shared memory layout (offsets from a 1024-aligned base)
     static constexpr int OFF_K = 0;
     // byte offset of d-chunk c of K slot s: paired slots interleave their chunks so the
@@ -155,7 +165,8 @@ __device__ __forceinline__ int pf_item(int k) {
 template <int D>
 __global__ void __launch_bounds__(kPfThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_q, float* __restrict__ o,
+                  const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
+                  float* __restrict__ o,
                   int B, int S, int H, int Hk, int causal, const int* __restrict__ seq_lens, float scale_log2,
                   int n_qtiles, int n_work, unsigned int* __restrict__ flags) {
     using C = PfCfg<D>;
@@ -209,6 +220,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_o);
     }
     tc_fence_before();
     __syncthreads();
@@ -219,23 +231,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     // counter (g) across items, so ring slots and barrier phases continue from item to
     // item.  Items without visible keys use no barrier at all.
     if (warp == 0) {
-        // ================================================================ K and V producers
-        // lane 0 streams the query and K tiles, lane 16 the V tiles (all by TMA, same box shape)
-        if (lane == 0 || lane == 16) {
-            const bool is_k = lane == 0;
-            const int NS = is_k ? C::NK : C::NV;
-            const uint32_t empty0 = is_k ? bar.k_empty : bar.v_empty;
-            const uint32_t full0 = is_k ? bar.k_full : bar.v_loaded;
-            const int off0 = is_k ? C::OFF_K : C::OFF_V;
-            const void* tm = is_k ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
-            int gs = 0;                   // fills of this ring so far
+        // ================================================================ K producer
+        // lane 0: per item [pad] the query tile (QSLOTS fills) then one K tile per block, by TMA.
+        // With paired slots the query fills must start on an even fill; an empty pad fill (a
+        // plain arrival, no data) restores that after an odd block count.
+        if (lane == 0) {
+            int gs = 0;                   // fills of the K ring so far
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int u = pf_item(k);
                 if (u >= n_work) break;
                 const PfWork w = work(u);
                 if (w.nblk == 0) continue;
-                if (is_k) {         // the next item's query tile -> L2, ahead of its own copy
+                {                   // the next item's query tile -> L2, ahead of its own copy
                     const int un = pf_item(k + 1);
                     if (un < n_work) {
                         const PfWork wn = work(un);
@@ -246,35 +254,93 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                                 tma_prefetch_l2_3d(&tm_q, wn.h * D + c * C::CH, wn.q0 + i * BN, wn.b);
                     }
                 }
-                // K ring: [pad] the item's query tile (QSLOTS fills, j < 0), then its K tiles.
-                // With paired slots the query fills must start on an even fill; an empty pad
-                // fill (a plain arrival, no data) restores that after an odd block count.
-                const bool pad = is_k && C::KPAIR && (gs & 1);
-                const int nq = is_k ? C::QSLOTS : 0;
+                const bool pad = C::KPAIR && (gs & 1);
+                constexpr int nq = C::QSLOTS;
                 for (int j = -nq - (pad ? 1 : 0); j < w.nblk; ++j) {
-                    const int s = gs % NS;
-                    if (!(ok = mbar_wait(empty0 + 8 * s, ((uint32_t)(gs / NS) & 1u) ^ 1u, abort_flag, flags))) break;
-                    const uint32_t full = full0 + 8 * s;
+                    const int s = gs % C::NK;
+                    if (!(ok = mbar_wait(bar.k_empty + 8 * s, ((uint32_t)(gs / C::NK) & 1u) ^ 1u, abort_flag, flags)))
+                        break;
+                    const uint32_t full = bar.k_full + 8 * s;
                     ++gs;
                     if (j < -nq) {          // pad fill
                         mbar_arrive(full);
                         continue;
                     }
                     mbar_arrive_expect_tx(full, C::TILE);
-                    const uint32_t dst = smem_addr(smem + off0);
                     const bool qfill = j < 0;
-                    const void* map = qfill ? static_cast<const void*>(&tm_q) : tm;
+                    const void* map = qfill ? static_cast<const void*>(&tm_q) : static_cast<const void*>(&tm_k);
                     const int x0 = (qfill ? w.h : w.g) * D;
                     const int y0 = qfill ? w.q0 + (j + nq) * BN : j * BN;
 #pragma unroll
                     for (int c = 0; c < C::NCH; ++c)
-                        tma_load_3d(dst + (is_k ? C::koff(s, c) : s * C::TILE + c * BN * C::CH * 4), map,
-                                    x0 + c * C::CH, y0, w.b, full);
+                        tma_load_3d(smem_addr(smem + C::OFF_K) + C::koff(s, c), map, x0 + c * C::CH, y0, w.b, full);
                 }
             }
             if (*abort_flag) {   // unwinding: let issued copies land
-                for (int f = max(0, gs - NS); f < gs; ++f)
-                    mbar_drain(full0 + 8 * (f % NS), (uint32_t)(f / NS) & 1u, 100000000ull);
+                for (int f = max(0, gs - C::NK); f < gs; ++f)
+                    mbar_drain(bar.k_full + 8 * (f % C::NK), (uint32_t)(f / C::NK) & 1u, 100000000ull);
+            }
+        }
+    } else if (warp == kPfVProdWarp) {
+        // ================================================================ V producer / O stores
+        // lane 0: per item one V tile per block by TMA, then OSLOTS output staging fills: no
+        // data, the slot is handed (plain arrival on v_loaded) to the epilogue, which writes
+        // O / l there and arrives on v_full.  This thread then stores the staged tile to the
+        // output by TMA and, once the copy engine has read it, releases the slots.  It does
+        // so before the first later fill that reuses one of them (or at the end).
+        if (lane == 0) {
+            int gs = 0;                   // fills of the V ring so far
+            bool ok = true;
+            int pend = -1;                // first staging fill not yet stored (-1: none)
+            PfWork pw{};                  // its item
+            auto flush = [&]() -> bool {
+                for (int i = 0; i < C::OSLOTS; ++i)
+                    if (!mbar_wait(bar.v_full + 8 * ((pend + i) % C::NV), (uint32_t)((pend + i) / C::NV) & 1u,
+                                   abort_flag, flags))
+                        return false;
+                for (int i = 0; i < C::OSLOTS; ++i) {
+                    const uint32_t src = smem_addr(smem + C::OFF_V) + ((pend + i) % C::NV) * C::TILE;
+#pragma unroll
+                    for (int cc = 0; cc < C::OCH; ++cc)
+                        tma_store_3d(&tm_o, src + cc * (kPfBM * C::CH * 4), pw.h * D + (i * C::OCH + cc) * C::CH,
+                                     pw.q0, pw.b);
+                }
+                bulk_commit();
+                bulk_wait_read_all();
+                for (int i = 0; i < C::OSLOTS; ++i) mbar_arrive(bar.v_empty + 8 * ((pend + i) % C::NV));
+                pend = -1;
+                return true;
+            };
+            for (int k = 0; ok; ++k) {
+                const int u = pf_item(k);
+                if (u >= n_work) break;
+                const PfWork w = work(u);
+                if (w.nblk == 0) continue;
+                for (int j = 0; j < w.nblk + C::OSLOTS; ++j) {
+                    if (pend >= 0 && gs >= pend + C::NV && !(ok = flush())) break;
+                    const int s = gs % C::NV;
+                    if (!(ok = mbar_wait(bar.v_empty + 8 * s, ((uint32_t)(gs / C::NV) & 1u) ^ 1u, abort_flag, flags)))
+                        break;
+                    const uint32_t full = bar.v_loaded + 8 * s;
+                    if (j >= w.nblk) {      // output staging fill
+                        if (j == w.nblk) { pend = gs; pw = w; }
+                        ++gs;
+                        mbar_arrive(full);
+                        continue;
+                    }
+                    ++gs;
+                    mbar_arrive_expect_tx(full, C::TILE);
+#pragma unroll
+                    for (int c = 0; c < C::NCH; ++c)
+                        tma_load_3d(smem_addr(smem + C::OFF_V) + s * C::TILE + c * BN * C::CH * 4, &tm_v,
+                                    w.g * D + c * C::CH, j * BN, w.b, full);
+                }
+            }
+            if (ok && pend >= 0) ok = flush();
+            bulk_wait_all();                  // output stores complete before the CTA exits
+            if (*abort_flag) {   // unwinding: let issued copies land
+                for (int f = max(0, gs - C::NV); f < gs; ++f)
+                    mbar_drain(bar.v_loaded + 8 * (f % C::NV), (uint32_t)(f / C::NV) & 1u, 100000000ull);
             }
         }
     } else if (warp == 1 || warp == kPfPvWarp) {
@@ -290,6 +356,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             bool ok = true;
             int issued_any = 0, g0 = 0, t = 0;   // t: items with keys so far
             int f = 0;                           // K-ring fills consumed (QK^T issuer)
+            int fv = 0;                          // V-ring fills passed (PV issuer)
             // Descriptors are built once; a k step or ring stage only adds its byte offset
             // (>> 4) to the start-address field, which cannot carry out of it (shared
             // addresses are below 2^18).
@@ -373,11 +440,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     if (t > 0) ok = mbar_wait(bar.o_free, (uint32_t)(t - 1) & 1u, abort_flag, flags);
                     for (int j = 0; ok && j < w.nblk; ++j) {
                         // O += P_gb V_gb
-                        const int gb = g0 + j;
-                        const int sv = gb % C::NV, sb = gb % C::NSBUF;
+                        const int gb = g0 + j, vf = fv + j;
+                        const int sv = vf % C::NV, sb = gb % C::NSBUF;
                         if (!(ok = mbar_wait(bar.p_ready + 8 * sb, (uint32_t)(gb / C::NSBUF) & 1u, abort_flag, flags)))
                             break;
-                        if (!(ok = mbar_wait(bar.v_full + 8 * sv, (uint32_t)(gb / C::NV) & 1u, abort_flag, flags)))
+                        if (!(ok = mbar_wait(bar.v_full + 8 * sv, (uint32_t)(vf / C::NV) & 1u, abort_flag, flags)))
                             break;
                         tc_fence_after();
                         const uint64_t vd = vdesc0 + (uint64_t)(sv * (C::TILE >> 4));
@@ -397,6 +464,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     }
                     if (!ok) break;
                     mma_commit(bar.o_final);
+                    fv += w.nblk + C::OSLOTS;          // the item's V tiles and output staging fills
                 }
                 g0 += w.nblk;
                 ++t;
@@ -432,7 +500,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 return key * 64 + (((dq & 3) ^ ((key >> 1) & 3)) << 4);
         };
         bool ok = true;
-        int gb = 0;                                          // V tiles consumed
+        int gb = 0;                                          // V-ring fills passed
         for (int k = 0; ok; ++k) {
             const int u = pf_item(k);
             if (u >= n_work) break;
@@ -480,6 +548,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 fence_proxy_async();          // generic-proxy stores -> tensor-core reads
                 mbar_arrive(bar.v_full + 8 * s);
             }
+            gb += C::OSLOTS;                                 // output staging fills: the epilogue's
         }
     } else {
         // ================================================================ softmax / epilogue
@@ -487,7 +556,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         const int r = quad * 32 + lane;                  // query row within the tile
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         bool ok = true;
-        int g0 = 0, t = 0;
+        int g0 = 0, t = 0, fv = 0;     // blocks, items with keys, V-ring fills passed
         for (int k = 0; ok; ++k) {
             const int u = pf_item(k);
             if (u >= n_work) break;
@@ -590,69 +659,62 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             }
             if (!ok) break;
             // ---------------------------------------------------------- epilogue
+            // O / l goes to the item's output staging fills (after its V tiles in the V
+            // ring); the V producer stores them to the output by TMA.
             ok = mbar_wait(bar.o_final, (uint32_t)t & 1u, abort_flag, flags);
             if (!(ok = __all_sync(0xffffffffu, ok))) break;
             tc_fence_after();
             const float inv = (qi < w.len && l_run > 0.0f) ? 1.0f / l_run : 0.0f;
-            // One row per lane would make every 16-byte store touch 32 rows.  Each group of
-            // NF lanes instead swaps NF x NF blocks of float4 (a butterfly over the low lane
-            // bits), after which lane gl holds float4 gl of the group's rows, and one store
-            // writes 32/NF whole row segments of 16*NF contiguous bytes.
-            constexpr int NF = D >= 32 ? 8 : 4;                 // float4 per row per chunk
-            const int gl = lane & (NF - 1);
-            const int grow0 = w.q0 + quad * 32 + (lane & ~(NF - 1));   // first row of the group
+            const int fs = fv + w.nblk;                          // first staging fill
+#pragma unroll 1
+            for (int i = 0; ok && i < C::OSLOTS; ++i) {
+                ok = mbar_wait(bar.v_loaded + 8 * ((fs + i) % C::NV), (uint32_t)((fs + i) / C::NV) & 1u, abort_flag,
+                               flags);
+                if (!(ok = __all_sync(0xffffffffu, ok))) break;
+                unsigned char* stage = smem + C::OFF_V + ((fs + i) % C::NV) * C::TILE;
 #pragma unroll
-            for (int c = 0; c < D / (4 * NF); ++c) {
-                uint32_t wv[4 * NF];
-                if constexpr (NF == 8) {
-                    tmem_ld32(lane_base + kColO + 32 * c, wv);
-                } else {
-                    tmem_ld16(lane_base + kColO, wv);
-                }
-                if constexpr (C::PV_SPLIT == 2) {                  // O = O_a + O_b
-                    uint32_t w2[4 * NF];
-                    if constexpr (NF == 8) {
-                        tmem_ld32(lane_base + kColO + D + 32 * c, w2);
+                for (int cc = 0; cc < C::OCH; ++cc) {
+                    const int c = i * C::OCH + cc;               // column chunk of O
+                    unsigned char* dst = stage + cc * (kPfBM * C::CH * 4);
+                    if constexpr (C::CH == 32) {
+                        uint32_t wv[32];
+                        tmem_ld32(lane_base + kColO + 32 * c, wv);
+                        if constexpr (C::PV_SPLIT == 2) {            // O = O_a + O_b
+                            uint32_t w2[32];
+                            tmem_ld32(lane_base + kColO + D + 32 * c, w2);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                wv[e] = __float_as_uint(__uint_as_float(wv[e]) + __uint_as_float(w2[e]));
+                        } else {
+                            tmem_wait_ld();
+                        }
+                        // 128-byte rows, 16-byte chunk index XOR row bits (the TMA box swizzle)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            *reinterpret_cast<float4*>(dst + r * 128 + (((e & 7) ^ (r & 7)) << 4)) =
+                                make_float4(__uint_as_float(wv[4 * e]) * inv, __uint_as_float(wv[4 * e + 1]) * inv,
+                                            __uint_as_float(wv[4 * e + 2]) * inv, __uint_as_float(wv[4 * e + 3]) * inv);
                     } else {
-                        tmem_ld16(lane_base + kColO + D, w2);
-                    }
-                    tmem_wait_ld();
+                        uint32_t wv[16], w2[16];
+                        tmem_ld16(lane_base + kColO, wv);
+                        tmem_ld16(lane_base + kColO + D, w2);      // D = 16 always splits PV
+                        tmem_wait_ld();
+                        // 64-byte rows, 64-byte swizzle
 #pragma unroll
-                    for (int e = 0; e < 4 * NF; ++e)
-                        wv[e] = __float_as_uint(__uint_as_float(wv[e]) + __uint_as_float(w2[e]));
-                } else {
-                    tmem_wait_ld();
-                }
-                float4 v[NF];
-#pragma unroll
-                for (int e = 0; e < NF; ++e)
-                    v[e] = make_float4(__uint_as_float(wv[4 * e]) * inv, __uint_as_float(wv[4 * e + 1]) * inv,
-                                       __uint_as_float(wv[4 * e + 2]) * inv, __uint_as_float(wv[4 * e + 3]) * inv);
-#pragma unroll
-                for (int bit = NF / 2; bit >= 1; bit >>= 1) {
-                    const bool up = (lane & bit) != 0;
-#pragma unroll
-                    for (int e = 0; e < NF; ++e) {
-                        if (e & bit) continue;
-                        // lanes without `bit` give element e|bit and take the partner's e (and
-                        // the converse), swapping the off-diagonal bit-blocks
-                        const float4 give = up ? v[e] : v[e | bit];
-                        float4 got;
-                        got.x = __shfl_xor_sync(0xffffffffu, give.x, bit);
-                        got.y = __shfl_xor_sync(0xffffffffu, give.y, bit);
-                        got.z = __shfl_xor_sync(0xffffffffu, give.z, bit);
-                        got.w = __shfl_xor_sync(0xffffffffu, give.w, bit);
-                        if (up) v[e] = got; else v[e | bit] = got;
+                        for (int e = 0; e < 4; ++e)
+                            *reinterpret_cast<float4*>(dst + r * 64 + (((e & 3) ^ ((r >> 1) & 3)) << 4)) = make_float4(
+                                (__uint_as_float(wv[4 * e]) + __uint_as_float(w2[4 * e])) * inv,
+                                (__uint_as_float(wv[4 * e + 1]) + __uint_as_float(w2[4 * e + 1])) * inv,
+                                (__uint_as_float(wv[4 * e + 2]) + __uint_as_float(w2[4 * e + 2])) * inv,
+                                (__uint_as_float(wv[4 * e + 3]) + __uint_as_float(w2[4 * e + 3])) * inv);
                     }
                 }
-#pragma unroll
-                for (int m = 0; m < NF; ++m) {
-                    const int row = grow0 + m;
-                    if (row < S)    // streaming: written once, not re-read here
-                        __stcs(reinterpret_cast<float4*>(o + ((int64_t)w.b * S + row) * q_row + (int64_t)w.h * D) +
-                                   c * NF + gl, v[m]);
-                }
+                fence_proxy_async();                             // generic stores -> TMA reads
+                mbar_arrive(bar.v_full + 8 * ((fs + i) % C::NV));
             }
+            if (!ok) break;
+            fv += w.nblk + C::OSLOTS;
             tc_fence_before();
             mbar_arrive(bar.o_free);     // O may be overwritten by the next item's first PV
             g0 += w.nblk;
@@ -688,7 +750,7 @@ static rkv_status launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream)
     using C = PfCfg<D>;
     auto encode = tensor_map_encoder();
     if (!encode) return set_error(RKV_ERR_LAUNCH, "attn_prefill: cuTensorMapEncodeTiled unavailable");
-    CUtensorMap tm_k, tm_v, tm_q;
+    CUtensorMap tm_k, tm_v, tm_q, tm_o;
     const cuuint64_t dims[3] = {(cuuint64_t)a.Hk * D, (cuuint64_t)a.S, (cuuint64_t)a.B};
     const cuuint64_t strides[2] = {(cuuint64_t)a.Hk * D * 4, (cuuint64_t)a.S * a.Hk * D * 4};
     const cuuint32_t box[3] = {(cuuint32_t)C::CH, (cuuint32_t)C::BN, 1};
@@ -708,6 +770,13 @@ static rkv_status launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream)
         cr = encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(a.q), qdims, qstrides, qbox, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        // output: same shape as the query; one staged column chunk of a whole tile per store
+        // (rows past the sequence end are clipped by the copy engine)
+        const cuuint32_t obox[3] = {(cuuint32_t)C::CH, (cuuint32_t)kPfBM, 1};
+        if (cr == CUDA_SUCCESS)
+            cr = encode(&tm_o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.o, qdims, qstrides, obox, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     if (cr != CUDA_SUCCESS) return set_error(RKV_ERR_LAUNCH, "attn_prefill: tensor map encode failed (%d)", (int)cr);
     auto kern = prefill_tc_kernel<D>;
@@ -726,7 +795,7 @@ static rkv_status launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream)
     const int sms = sm_count();
     if (sms <= 0) return set_error(RKV_ERR_LAUNCH, "attn_prefill: cannot query the SM count");
     const int grid = (int)(n_work < (int64_t)sms ? n_work : (int64_t)sms);
-    kern<<<grid, kPfThreads, C::SMEM, stream>>>(tm_k, tm_v, tm_q, a.o, a.B, a.S, a.H, a.Hk, a.causal ? 1 : 0,
+    kern<<<grid, kPfThreads, C::SMEM, stream>>>(tm_k, tm_v, tm_q, tm_o, a.o, a.B, a.S, a.H, a.Hk, a.causal ? 1 : 0,
                                                 a.seq_lens, a.scale * kPfLog2e, n_qtiles, (int)n_work, a.flags);
     return check_launch("attn_prefill");
 }
