@@ -179,6 +179,9 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
             int it = 0;
             bool ok = true;
             int64_t pos = r0;
+            // K/V rows are read once per step: evict-first in L2, so the stream does not push
+            // out (and force the write-back of) lines other kernels left dirty.
+            const uint64_t stream_policy = l2_policy_evict_first();
             while (ok && pos < r1) {
                 int m, kh;
                 int64_t seg_start;
@@ -194,8 +197,10 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
                     const uint32_t full = smem_addr(&bars[s]);
                     mbar_arrive_expect_tx(full, 2 * bytes);
                     const int64_t src = (head_row0 + t0) * D;
-                    bulk_g2s(smem_addr(smem + C::OFF_STAGES + (2 * s) * C::TILE_BYTES), k_cache + src, bytes, full);
-                    bulk_g2s(smem_addr(smem + C::OFF_STAGES + (2 * s + 1) * C::TILE_BYTES), v_cache + src, bytes, full);
+                    bulk_g2s_hint(smem_addr(smem + C::OFF_STAGES + (2 * s) * C::TILE_BYTES), k_cache + src, bytes, full,
+                                  stream_policy);
+                    bulk_g2s_hint(smem_addr(smem + C::OFF_STAGES + (2 * s + 1) * C::TILE_BYTES), v_cache + src, bytes,
+                                  full, stream_policy);
                     issued[s] = it + 1;
                 }
                 pos = piece_end;
