@@ -53,6 +53,7 @@ def parse_args():
     p.add_argument("--impl", choices=["rkv", "reference"], default="rkv")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-configs", action="store_true", help="skip the per-workload lines")
     return p.parse_args()
 
 
@@ -303,11 +304,103 @@ def run_rkv(args, rank, world, torch, dist):
         "gpu_launches": LAUNCHES_PER_STEP * K,
         "clocks": clocks,
     }
+    if not args.no_configs:
+        main = {"prefill_tflops": prefill_tflops, "prefill_ms": prefill_ms,
+                "fill_gbs": rooflines["scatter_fill"]["achieved"], "decode_step_gbs": decode_step_gbs,
+                "decode_step_ms": dsc_ms + dec_ms}
+        out["configs"], _ = measure_configs(torch, rkv, dev, stream, main, peaks, peak_kind)
+        if rkv.rkv_read_device_flags() & rkv.RKV_FLAG_WAIT_TIMEOUT:
+            raise RuntimeError("device reported a wait timeout during the per-workload runs")
     if not args.no_e2e:
         out["e2e"] = run_e2e(W, torch, rkv, stream, K=max(3, min(K, 10)))
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         out["cpu_baseline"] = cpu_baseline(W.host_decode, W.host_prefill)
     return out
+
+
+class L2Flush:
+    """Writes a buffer twice the size of L2 so the next launch starts from HBM."""
+
+    def __init__(self, torch, dev, nbytes=256 << 20):
+        self.buf = torch.empty(nbytes // 4, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.buf.fill_(1.0)
+
+
+def time_launches(torch, stream, fn, iters, flush=None):
+    """Mean device time (ms) of fn() over `iters` launches, each bracketed by CUDA events on
+    the launching stream; with `flush`, L2 is flushed before every launch (outside the events)."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for a, b in evs:
+        if flush is not None:
+            flush()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return float(np.mean([a.elapsed_time(b) for a, b in evs]))
+
+
+def measure_configs(torch, rkv, dev, stream, main, peaks, peak_kind):
+    """Throughput and roofline fraction of each of the five workloads at one GPU.
+
+    The causal GQA prefill + cache fill and the batched decode step come from the main timed
+    loop (`main`); the tiny and encoder prefills are timed here launch by launch with L2
+    flushed before each launch (their inputs fit in L2); the long-context decode runs its 256
+    append+decode steps back to back (its 268 MB cache is larger than L2)."""
+    hbm = peaks["hbm_gbs"]
+    tf32 = peaks["bf16_tflops"] * TF32_PER_BF16
+    flush = L2Flush(torch, dev)
+    out = {}
+    for shape, iters in ((inputs.TINY, 200), (inputs.ENCODER, 50)):
+        q, k, v = (torch.from_numpy(a).to(dev) for a in inputs.prefill_inputs(shape))
+        o = torch.empty_like(q)
+        run = lambda: rkv.attn_prefill(q, k, v, o, shape.B, shape.S, shape.H, shape.Hk, shape.D, shape.causal)
+        for _ in range(3):
+            run()
+        ms = time_launches(torch, stream, run, iters, flush)
+        tfl = shape.flops / (ms * 1e-3) / 1e12
+        out[shape.name] = {"value": tfl, "unit": "TFLOP/s", "ms": ms, "bound": "tensor", "peak": tf32,
+                           "frac": tfl / tf32, "launches": iters, "l2": "flushed before each launch"}
+    out[inputs.TINY.name]["note"] = "launch-latency bound (131 kFLOP); not a roofline case"
+    out[PREFILL.name + " + cache fill"] = {
+        "value": main["prefill_tflops"], "unit": "TFLOP/s", "ms": main["prefill_ms"], "bound": "tensor",
+        "peak": tf32, "frac": main["prefill_tflops"] / tf32,
+        "cache_fill_gbs": main["fill_gbs"], "cache_fill_frac": main["fill_gbs"] / hbm}
+    out[DECODE.name] = {"value": main["decode_step_gbs"], "unit": "GB/s", "bound": "hbm", "peak": hbm,
+                        "frac": main["decode_step_gbs"] / hbm, "ms": main["decode_step_ms"],
+                        "note": "K/V rows attended / (new-row scatter + decode)"}
+    d = inputs.LONG_DECODE
+    H, Hk, D, L, T = d.H, d.Hk, d.D, d.Lmax, d.extra["steps"]
+    kc = torch.from_numpy(inputs.normal((1, Hk, L, D), inputs.SEED_K)).to(dev)
+    vc = torch.from_numpy(inputs.normal((1, Hk, L, D), inputs.SEED_V)).to(dev)
+    steps = [inputs.long_decode_step_inputs(t) for t in range(T)]
+    qs = torch.from_numpy(np.stack([x["q"] for x in steps])).to(dev)          # [T,1,H*D]
+    kn = torch.from_numpy(np.stack([x["k_new"] for x in steps])).to(dev)      # [T,1,1,Hk*D]
+    vn = torch.from_numpy(np.stack([x["v_new"] for x in steps])).to(dev)
+    pos = torch.tensor([x["pos"] for x in steps], dtype=torch.int32, device=dev)
+    lens = torch.tensor([x["len"] for x in steps], dtype=torch.int32, device=dev)
+    od = torch.empty((1, H * D), device=dev)
+    nws = rkv.attn_decode_workspace_bytes(1, H, Hk, D, L)
+    ws = torch.zeros(nws, dtype=torch.uint8, device=dev)
+
+    def run_long():
+        for t in range(T):
+            rkv.kv_cache_scatter(kn[t], vn[t], kc, vc, 1, 1, Hk, D, L, pos[t:t + 1])
+            rkv.attn_decode_batched(qs[t], kc, vc, od, 1, H, Hk, D, L, lens[t:t + 1], 0.0, ws, nws)
+
+    run_long()
+    ms = time_launches(torch, stream, run_long, 3)
+    kv = sum(2.0 * Hk * x["len"] * D * 4 for x in steps)
+    gbs = kv / (ms * 1e-3) / 1e9
+    out[d.name] = {"value": gbs, "unit": "GB/s", "ms": ms, "bound": "hbm", "peak": hbm, "frac": gbs / hbm,
+                   "launches": 2 * T, "note": f"256 append+decode steps, {kv / 1e9:.2f} GB of K/V rows read; "
+                   "per-step launches back to back on one stream"}
+    for v in out.values():
+        v["peak_note"] = f"{peak_kind} " + ("copy bandwidth" if v["bound"] == "hbm" else
+                                            "bf16 burst x nominal TF32/BF16 ratio 1.1/2.25")
+    return out, 2 * T
 
 
 def run_e2e(W, torch, rkv, stream, K):
