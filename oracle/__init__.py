@@ -14,6 +14,10 @@ Page citations are in the C file's header; the functions here follow it:
               cache layout from realizar cache_from_cache_from_kv_cache.rs,
               fn init_batched_kv_cache_gpu.
   scatter  -- trueno-gpu attention.rs, fn kv_cache_scatter_gpu.
+  prefill_cached -- a prefill appended behind an existing cache, which
+              trustformers-core attention.rs, fn attention_prefill_gpu_to_gpu
+              says must run the decode path once per token: query i of the
+              chunk sees cache rows 0..start_pos+i.
 """
 from __future__ import annotations
 
@@ -75,8 +79,10 @@ def _configure(lib):
     lib.rkv_oracle_prefill_probs.argtypes = [P, P, P, I, I, I, I, I, I, P, D, I, I, I, P]
     lib.rkv_oracle_decode.argtypes = [P, P, P, P, I, I, I, I, I, P, D]
     lib.rkv_oracle_scatter.argtypes = [P, P, P, P, I, I, I, I, I, P, P]
+    lib.rkv_oracle_prefill_cached.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P, P, D]
     for f in ("rkv_oracle_prefill", "rkv_oracle_prefill_rows", "rkv_oracle_prefill_probs",
-              "rkv_oracle_decode", "rkv_oracle_scatter", "rkv_oracle_num_threads"):
+              "rkv_oracle_decode", "rkv_oracle_scatter", "rkv_oracle_num_threads",
+              "rkv_oracle_prefill_cached"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -177,3 +183,19 @@ def scatter(k_new, v_new, k_cache, v_cache, M, T, Hk, D, Lmax, start_pos, inplac
     if rc != 0:
         raise ValueError("oracle scatter rejected its arguments")
     return kc, vc, int(ov[0])
+
+
+def prefill_cached(q, k_cache, v_cache, B, T, H, Hk, D, Lmax, causal, start_pos, q_lens=None,
+                   scale=None):
+    """O[B, T, H*D] (float64): a chunk of T queries per sequence at positions start_pos[b]+i
+    against cache [B,Hk,Lmax,D] that already holds the chunk's own K/V rows."""
+    q, kc, vc = _f32(q), _f32(k_cache), _f32(v_cache)
+    assert q.size == B * T * H * D and kc.size == B * Hk * Lmax * D and vc.size == kc.size
+    sp, ql = _i32(start_pos), _i32(q_lens)
+    o = np.zeros((B, T, H * D), dtype=np.float64)
+    rc = _load().rkv_oracle_prefill_cached(_ptr(q), _ptr(kc), _ptr(vc), _ptr(o), B, T, H, Hk, D, Lmax,
+                                           int(bool(causal)), _ptr(sp), _ptr(ql),
+                                           default_scale(D) if scale is None else float(scale))
+    if rc != 0:
+        raise ValueError("oracle prefill_cached rejected its arguments (start + length above max_len?)")
+    return o

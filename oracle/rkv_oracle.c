@@ -275,3 +275,62 @@ int rkv_oracle_scatter(const float* k_new, const float* v_new, float* k_c, float
     if (overflow) *overflow += skipped;
     return 0;
 }
+
+/*
+ * Prefill appended behind rows already in the batched cache (chunked prefill).
+ *
+ * trustformers-core attention.rs, fn attention_prefill_gpu_to_gpu states that
+ * its causal mask is the from-empty-cache one and that a prefill appended to
+ * an existing cache must instead run the decode path once per token
+ * (fn attention_decode_gpu_to_gpu: one query against every cached row, no
+ * mask).  That per-token rule is what this function computes, for a chunk of
+ * T query tokens whose own K/V rows are already in the cache:
+ *   query i of sequence b sits at position p0 = start_pos[b] plus i and, like
+ *   a decode step of length p0 + i + 1, sees cache rows 0 .. p0+i (causal);
+ *   non-causal, every valid query sees rows 0 .. p0+n-1.
+ *   q, o      : [B, T, H*D]
+ *   k_c, v_c  : [B, Hk, Lmax, D]
+ *   start_pos : int[B], rows in the cache before the chunk
+ *   q_lens    : int[B] valid query rows n of the chunk (<= T), or NULL for T;
+ *               rows i >= n are zero.
+ * Returns -1 on invalid shapes, a negative start or p0 + n > Lmax.
+ */
+int rkv_oracle_prefill_cached(const float* q, const float* k_c, const float* v_c, double* o,
+                              int B, int T, int H, int Hk, int D, int Lmax, int causal,
+                              const int* start_pos, const int* q_lens, double scale)
+{
+    if (B < 0 || T < 0 || H <= 0 || Hk <= 0 || D <= 0 || Lmax <= 0 || H % Hk != 0) return -1;
+    for (int b = 0; b < B; ++b) {
+        const int n = q_lens ? q_lens[b] : T;
+        if (start_pos[b] < 0 || n < 0 || n > T || (int64_t)start_pos[b] + n > Lmax) return -1;
+    }
+    const int64_t q_row = (int64_t)H * D;
+    const int64_t n_rows = (int64_t)B * H * T;
+    int rc = 0;
+#pragma omp parallel
+    {
+        double* scores = (double*)malloc(sizeof(double) * (size_t)Lmax);
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < n_rows; ++r) {
+            if (!scores) {
+#pragma omp atomic write
+                rc = -1;
+                continue;
+            }
+            const int b = (int)(r / ((int64_t)H * T));
+            const int h = (int)((r / T) % H);
+            const int i = (int)(r % T);
+            const int p0 = start_pos[b];
+            const int n = q_lens ? q_lens[b] : T;
+            int n_keys = 0;                       /* padded query row -> zero output */
+            if (i < n) n_keys = causal ? p0 + i + 1 : p0 + n;
+            const int g = kv_head_of(h, H, Hk);
+            const int64_t head_base = (((int64_t)b * Hk + g) * Lmax) * D;
+            const int64_t at = ((int64_t)b * T + i) * q_row + (int64_t)h * D;
+            attend_row(q + at, k_c + head_base, v_c + head_base, D, D, n_keys, D, scale, scores,
+                       o + at, NULL);
+        }
+        free(scores);
+    }
+    return rc;
+}

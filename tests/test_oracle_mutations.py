@@ -29,6 +29,11 @@ MUTATIONS = {
     "scatter_head_stride": ("* Hk * D + (int64_t)kh * D;", "* Hk * D;"),
     "query_head_offset": ("* q_row + (int64_t)h * D;\n            const float* kb",
                           "* q_row;\n            const float* kb"),
+    "chunk_causal_off_by_one": ("n_keys = causal ? p0 + i + 1 : p0 + n;", "n_keys = causal ? p0 + i : p0 + n;"),
+    "chunk_ignores_start": ("n_keys = causal ? p0 + i + 1 : p0 + n;", "n_keys = causal ? i + 1 : n;"),
+    "chunk_noncausal_sees_capacity": ("n_keys = causal ? p0 + i + 1 : p0 + n;",
+                                      "n_keys = causal ? p0 + i + 1 : Lmax;"),
+    "chunk_padded_rows_kept": ("if (i < n) n_keys", "if (i < T) n_keys"),
 }
 
 
@@ -47,6 +52,13 @@ def _pin_checks():
     checks.append(lambda: pins.test_decode_equals_last_row_of_causal_prefill(om))
     checks.append(lambda: pins.test_scatter_readback_identity_and_canaries(om))
     checks.append(lambda: pins.test_padded_query_rows_are_zero(om))
+    for causal in (False, True):
+        checks.append(lambda c=causal: pins.test_golden_prefill_cached(om, c))
+        checks.append(lambda c=causal: pins.test_prefill_cached_from_empty_cache_equals_prefill(om, c))
+    for ci in range(len(pins._CACHED_CASES)):
+        checks.append(lambda ci=ci: pins.test_prefill_cached_matches_brute_force(om, ci))
+    checks.append(lambda: pins.test_prefill_cached_single_token_equals_decode(om))
+    checks.append(lambda: pins.test_prefill_cached_chunks_compose_to_full_prefill(om))
     return checks
 
 

@@ -323,3 +323,123 @@ def test_scatter_readback_identity_and_canaries(oracle_mod):
             np.testing.assert_array_equal(vc[m, :, p, :], vn[m, t].reshape(Hk, D))
     assert np.array_equal(kc[~written], kc0[~written])
     assert np.array_equal(vc[~written], vc0[~written])
+
+
+# ------------------------------------------------- prefill behind an existing cache
+def brute_prefill_cached(q, kc, vc, B, T, H, Hk, D, L, causal, start_pos, q_lens=None, scale=None):
+    """Dense scores over the whole cache, a mask on absolute positions, scipy softmax."""
+    scale = 1.0 / np.sqrt(D) if scale is None else scale
+    q4 = np.asarray(q, np.float64).reshape(B, T, H, D)
+    grp = np.arange(H) // (H // Hk)
+    n_q = np.full(B, T) if q_lens is None else np.asarray(q_lens)
+    out = np.zeros((B, T, H, D))
+    pos_key = np.arange(L)[None, :]
+    for b in range(B):
+        kk = np.asarray(kc, np.float64)[b][grp]                  # [H, L, D]
+        vv = np.asarray(vc, np.float64)[b][grp]
+        sc = np.einsum("ihd,hjd->hij", q4[b], kk) * scale        # [H, T, L]
+        pos_q = start_pos[b] + np.arange(T)[:, None]              # absolute query positions
+        vis = (np.arange(T)[:, None] < n_q[b]) & (pos_key < start_pos[b] + n_q[b])
+        if causal:
+            vis &= pos_key <= pos_q
+        s = np.where(vis[None], sc, -np.inf)
+        with np.errstate(invalid="ignore"):
+            p = np.nan_to_num(np.where(vis[None], scipy_softmax(s, axis=-1), 0.0))
+        out[b] = np.einsum("hij,hjd->ihd", p, vv)
+    return out.reshape(B, T, H * D)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_golden_prefill_cached(oracle_mod, causal):
+    g = _golden("chunk_behind_cache_closed_form.json")
+    B, T, H, Hk, D, L = g["B"], g["T"], g["H"], g["Hk"], g["D"], g["Lmax"]
+    q = np.array(g["q"], np.float32).reshape(B, T, H * D)
+    kc = np.array(g["k_cache"], np.float32).reshape(B, Hk, L, D)
+    vc = np.array(g["v_cache"], np.float32).reshape(B, Hk, L, D)
+    o = oracle_mod.prefill_cached(q, kc, vc, B, T, H, Hk, D, L, causal, np.array(g["start_pos"]),
+                                  q_lens=np.array(g["q_lens"]), scale=g["scale"])
+    want = np.array(g["expected_causal" if causal else "expected_noncausal"], np.float64)
+    assert np.max(np.abs(o.reshape(want.shape) - want)) <= g["tolerance"]
+
+
+_CACHED_CASES = [
+    # B, T, H, Hk, D, L, causal, start_pos, q_lens
+    (1, 1, 1, 1, 1, 1, True, [0], None),
+    (1, 3, 2, 2, 3, 8, True, [5], None),
+    (1, 3, 2, 2, 3, 8, False, [5], None),
+    (2, 4, 4, 2, 4, 9, True, [0, 3], [4, 2]),
+    (3, 5, 6, 3, 2, 12, False, [7, 0, 2], [5, 0, 3]),
+    (2, 2, 4, 1, 4, 6, True, [4, 1], None),
+]
+
+
+@pytest.mark.parametrize("ci", range(len(_CACHED_CASES)))
+def test_prefill_cached_matches_brute_force(oracle_mod, ci):
+    B, T, H, Hk, D, L, causal, sp, ql = _CACHED_CASES[ci]
+    seed = 2000 + ci
+    q = inputs.normal((B, T, H * D), (seed, 0))
+    kc = inputs.normal((B, Hk, L, D), (seed, 1))
+    vc = inputs.normal((B, Hk, L, D), (seed, 2))
+    got = oracle_mod.prefill_cached(q, kc, vc, B, T, H, Hk, D, L, causal, np.array(sp), q_lens=ql)
+    want = brute_prefill_cached(q, kc, vc, B, T, H, Hk, D, L, causal, np.array(sp), q_lens=ql)
+    assert np.max(np.abs(got - want)) < 1e-12
+
+
+def _cache_of(k, v, B, S, Hk, D, L, fill=1e30):
+    """Caches [B,Hk,L,D] holding the interleaved rows k/v [B,S,Hk*D] at positions 0..S-1; the
+    rows after them hold `fill`, which would dominate any result that read them."""
+    kc = np.full((B, Hk, L, D), fill, np.float32)
+    vc = np.full((B, Hk, L, D), fill, np.float32)
+    kc[:, :, :S, :] = k.reshape(B, S, Hk, D).transpose(0, 2, 1, 3)
+    vc[:, :, :S, :] = v.reshape(B, S, Hk, D).transpose(0, 2, 1, 3)
+    return kc, vc
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_prefill_cached_from_empty_cache_equals_prefill(oracle_mod, causal):
+    """start_pos = 0: the chunk is the whole sequence, so the result is the ordinary prefill
+    (padding included: q_lens plays the role of seq_lens)."""
+    B, S, H, Hk, D = 2, 7, 4, 2, 4
+    q, k, v = (inputs.normal((B, S, n * D), (2101, t)) for t, n in enumerate((H, Hk, Hk)))
+    lens = np.array([7, 4])
+    kc, vc = _cache_of(k, v, B, S, Hk, D, S + 3)
+    for b in range(B):               # keys past a sequence's length are not part of it
+        kc[b, :, lens[b]:, :] = 1e30
+        vc[b, :, lens[b]:, :] = 1e30
+    got = oracle_mod.prefill_cached(q, kc, vc, B, S, H, Hk, D, S + 3, causal, np.zeros(B, np.int32),
+                                    q_lens=lens)
+    want = oracle_mod.prefill(q, k, v, B, S, H, Hk, D, causal, seq_lens=lens)
+    assert np.max(np.abs(got - want)) < 1e-12
+
+
+def test_prefill_cached_single_token_equals_decode(oracle_mod):
+    """T = 1: the chunk is one decode step of length start_pos + 1 (the page's per-token rule)."""
+    M, H, Hk, D, L = 3, 4, 2, 4, 10
+    q = inputs.normal((M, 1, H * D), (2201, 0))
+    kc = inputs.normal((M, Hk, L, D), (2201, 1))
+    vc = inputs.normal((M, Hk, L, D), (2201, 2))
+    sp = np.array([0, 6, 9], np.int32)
+    got = oracle_mod.prefill_cached(q, kc, vc, M, 1, H, Hk, D, L, True, sp)
+    want = oracle_mod.decode(q.reshape(M, H * D), kc, vc, M, H, Hk, D, L, sp + 1)
+    assert np.max(np.abs(got.reshape(M, H * D) - want)) < 1e-12
+
+
+def test_prefill_cached_chunks_compose_to_full_prefill(oracle_mod):
+    """A causal prefill of S tokens equals a first chunk of c tokens followed by a second chunk
+    of S - c tokens behind it (both reading the cache that holds all S rows)."""
+    B, S, H, Hk, D, c = 2, 9, 4, 1, 4, 4
+    q, k, v = (inputs.normal((B, S, n * D), (2301, t)) for t, n in enumerate((H, Hk, Hk)))
+    full = oracle_mod.prefill(q, k, v, B, S, H, Hk, D, True)
+    kc, vc = _cache_of(k, v, B, S, Hk, D, S + 2)
+    first = oracle_mod.prefill_cached(q[:, :c], kc, vc, B, c, H, Hk, D, S + 2, True, np.zeros(B, np.int32))
+    second = oracle_mod.prefill_cached(q[:, c:], kc, vc, B, S - c, H, Hk, D, S + 2, True,
+                                       np.full(B, c, np.int32))
+    assert np.max(np.abs(first - full[:, :c])) < 1e-12
+    assert np.max(np.abs(second - full[:, c:])) < 1e-12
+
+
+def test_prefill_cached_rejects_chunk_past_capacity(oracle_mod):
+    q = inputs.normal((1, 3, 4), 1)
+    kc = inputs.normal((1, 1, 5, 4), 2)
+    with pytest.raises(ValueError):
+        oracle_mod.prefill_cached(q, kc, kc, 1, 3, 1, 1, 4, 5, True, np.array([3]))
