@@ -127,7 +127,7 @@ def kernel_hash(*files):
     return h.hexdigest()[:16]
 
 
-KERNEL_FILES = {"prefill": ("prefill_tc.cu",), "decode": ("decode_splitkv.cu",), "scatter": ("kv_scatter.cu",)}
+KERNEL_FILES = {"prefill": ("prefill_tc.cuh", "prefill_tc.cu"), "decode": ("decode_splitkv.cu",), "scatter": ("kv_scatter.cu",)}
 
 
 def ncu_traffic(kernel):
@@ -364,6 +364,27 @@ def measure_configs(torch, rkv, dev, stream, main, peaks, peak_kind):
         out[shape.name] = {"value": tfl, "unit": "TFLOP/s", "ms": ms, "bound": "tensor", "peak": tf32,
                            "frac": tfl / tf32, "launches": iters, "l2": "flushed before each launch"}
     out[inputs.TINY.name]["note"] = "launch-latency bound (131 kFLOP); not a roofline case"
+    # chunked prefill: the causal GQA sequences' second 1024 tokens behind their first 1024 rows
+    P, L, c = PREFILL, FILL_LEN, PREFILL.S // 2
+    q, k, v = (torch.from_numpy(a).to(dev) for a in inputs.prefill_inputs(P))
+    kc = torch.zeros((P.B, P.Hk, L, P.D), device=dev)
+    vc = torch.zeros_like(kc)
+    rkv.kv_cache_scatter(k, v, kc, vc, P.B, P.S, P.Hk, P.D, L, torch.zeros(P.B, dtype=torch.int32, device=dev))
+    q2 = q[:, c:].contiguous()
+    o2 = torch.empty_like(q2)
+    start = torch.full((P.B,), c, dtype=torch.int32, device=dev)
+    run = lambda: rkv.attn_prefill_chunked(q2, kc, vc, o2, P.B, P.S - c, P.H, P.Hk, P.D, L, True, start)
+    for _ in range(3):
+        run()
+    ms = time_launches(torch, stream, run, 20, flush)
+    T = P.S - c
+    flops = 4.0 * P.B * P.H * P.D * (T * c + T * (T + 1) / 2)
+    tfl = flops / (ms * 1e-3) / 1e12
+    out[f"chunked causal GQA prefill B={P.B} T={T} behind {c} cached rows H={P.H} Hk={P.Hk} D={P.D} "
+        f"Lmax={L}"] = {"value": tfl, "unit": "TFLOP/s", "ms": ms, "bound": "tensor", "peak": tf32,
+                        "frac": tfl / tf32, "launches": 20, "l2": "flushed before each launch",
+                        "note": "attn_prefill_chunked; FLOP counted over the keys each token sees"}
+    del q, k, v, kc, vc, q2, o2
     out[PREFILL.name + " + cache fill"] = {
         "value": main["prefill_tflops"], "unit": "TFLOP/s", "ms": main["prefill_ms"], "bound": "tensor",
         "peak": tf32, "frac": main["prefill_tflops"] / tf32,

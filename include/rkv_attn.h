@@ -100,6 +100,37 @@ rkv_status attn_prefill(const float* q, const float* k, const float* v, float* o
                         int causal, const int* seq_lens, float scale, cudaStream_t stream);
 
 /*
+ * Prefill appended behind rows already in the resident cache (chunked prefill).
+ *
+ * Cites: trustformers-core attention.rs, fn attention_prefill_gpu_to_gpu (its
+ * doc: the causal mask is the from-empty-cache one, and a prefill appended to
+ * an existing cache must run the decode path once per token) and
+ * fn attention_decode_gpu_to_gpu (one query against every cached row).  This
+ * call computes that per-token result for a whole chunk in one launch.
+ *
+ *   q          [M, T, n_heads*head_dim]             input, T new tokens per sequence
+ *   k_cache,
+ *   v_cache    [M, n_kv_heads, max_len, head_dim]   input; must already hold the
+ *              chunk's own K/V rows at start_pos .. start_pos+n-1 (kv_cache_scatter)
+ *   o          [M, T, n_heads*head_dim]             output, fully written
+ *   start_pos  device int32[M]: p0, cache rows present before the chunk
+ *   q_lens     device int32[M]: valid tokens n of the chunk (<= T), or NULL for T;
+ *              rows i >= n are written as 0
+ *   causal     1: token i (position p0+i) sees cache rows 0..p0+i;
+ *              0: every valid token sees rows 0..p0+n-1
+ * Device values out of range are clamped and flagged: n > T or p0 + n > max_len
+ * (keys past max_len are not read; RKV_FLAG_LEN_CLAMPED), negative p0 or n
+ * (treated as 0; RKV_FLAG_NEGATIVE_INPUT).  Cache rows past p0+n are never
+ * used, even if they hold NaN.  Same kernel and arithmetic as attn_prefill
+ * (TF32 tensor cores, f32 accumulation; K/V tiles by tensor copies straight
+ * from the cache).  0 <= M <= 32, T <= max_len; o must not alias q or the caches.
+ */
+rkv_status attn_prefill_chunked(const float* q, const float* k_cache, const float* v_cache,
+                                float* o, int M, int T, int n_heads, int n_kv_heads,
+                                int head_dim, int max_len, int causal, const int* start_pos,
+                                const int* q_lens, float scale, cudaStream_t stream);
+
+/*
  * Bytes of device workspace attn_decode_batched needs for these sizes.
  * Returns 0 for invalid sizes.
  */

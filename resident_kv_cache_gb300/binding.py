@@ -65,6 +65,8 @@ def load():
     lib.rkv_read_device_flags.argtypes = [ctypes.POINTER(ctypes.c_uint), I, P]
     lib.attn_prefill.restype = I
     lib.attn_prefill.argtypes = [P, P, P, P, I, I, I, I, I, I, P, F, P]
+    lib.attn_prefill_chunked.restype = I
+    lib.attn_prefill_chunked.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P, P, F, P]
     lib.attn_decode_workspace_bytes.restype = SZ
     lib.attn_decode_workspace_bytes.argtypes = [I, I, I, I, I]
     lib.attn_decode_batched.restype = I
@@ -124,6 +126,13 @@ def attn_prefill(q, k, v, o, batch, seq_len, n_heads, n_kv_heads, head_dim, caus
     _check("attn_prefill", load().attn_prefill(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), batch, seq_len, n_heads, n_kv_heads, head_dim,
         int(bool(causal)), _ptr(seq_lens), float(scale), _stream(stream)))
+
+
+def attn_prefill_chunked(q, k_cache, v_cache, o, M, T, n_heads, n_kv_heads, head_dim, max_len, causal,
+                         start_pos, q_lens=None, scale=0.0, stream=None):
+    _check("attn_prefill_chunked", load().attn_prefill_chunked(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), M, T, n_heads, n_kv_heads, head_dim, max_len,
+        int(bool(causal)), _ptr(start_pos), _ptr(q_lens), float(scale), _stream(stream)))
 
 
 def attn_decode_workspace_bytes(M, n_heads, n_kv_heads, head_dim, max_len) -> int:

@@ -1,813 +1,25 @@
-// prefill_tc.cu -- fused flash-style prefill on the 5th-generation tensor core (sm_103a).
+// prefill_tc.cu -- launches of the tensor-core prefill (prefill_tc.cuh) for whole
+// sequences of interleaved activations, and the dispatch between the two variants.
 //
 // Semantics: trueno-gpu 0.4.11 src/memory/resident/attention.rs,
-// fn batched_multihead_attention_optimized (interleaved [seq, n_heads*head_dim]
-// in and out, scale 1/sqrt(head_dim)) and trustformers-core 0.2.0
-// src/gpu_ops/cuda/oxicuda/attention.rs, fn attention_prefill_gpu_to_gpu
-// (causal: query i sees keys 0..=i; per head: scaled GEMM, causal softmax,
-// GEMM).  Here all of it is one kernel: heads are read in place, the score
-// tile never leaves tensor memory, and softmax is online (base 2).
-//
-// The kernel is persistent: one CTA per SM walks a static list of work items (a
-// 128-query tile of one (batch, head)), heaviest causal tiles first, dealt in rounds
-// that alternate direction.  Rings, TMEM buffers and barrier phases run on across
-// items, so one item's prologue (Q load) and epilogue (O store) overlap the tensor-core
-// work of its neighbours.  Warp roles:
-//   warp 0       K producer (one thread): TMA (cp.async.bulk.tensor, 128-byte
-//                swizzle) of BN x D tiles into an NK-stage ring that carries each
-//                item's query tile ahead of its key tiles; it also prefetches the
-//                next item's query tile into L2.
-//   warp 11      V producer (one thread): V tiles into an NV-stage ring, followed per
-//                item by output staging slots that the epilogue fills with O / l and
-//                this thread stores to the output by TMA.
-//   warp 1       QK^T issuer (one thread) and TMEM owner: per item, Q goes from
-//                the K ring into TMEM by tcgen05.cp, then per key block
-//                  S_j = Q . K_j^T   tcgen05.mma kind::tf32, A = Q from TMEM
-//                S goes to NSBUF TMEM buffers, so QK^T runs up to NSBUF blocks
-//                ahead of the softmax.
-//   warp 10      PV issuer (one thread):  O += P_j . V_j, A = P from TMEM.
-//   warps 2-5    softmax / epilogue, one thread per query row (TMEM lane): per
-//                block: S row from TMEM, mask, row max, lazy rescale (O is
-//                rescaled only when the running max grows by more than 2^8),
-//                p = 2^(s*scale*log2e - m) truncated to TF32 and written back over
-//                S; per item: O / l written to the staging slots (swizzled like the
-//                TMA box, conflict-free).
-//   warps 6-9    V transposer: tcgen05 kind::tf32 reads B only K-major, so each
-//                V tile is transposed in shared memory (4x4 blocks through
-//                registers, conflict-free 16-byte stores, 128-byte swizzle).
-// Q, K and V stay f32; the tensor core reads them as TF32 by truncation.
-// Every mbarrier wait is time-bounded (see rkv_internal.cuh); a CTA that gives
-// up unwinds: it drains its own copies in flight, lets issued MMAs finish and
-// frees its TMEM.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include "rkv_internal.cuh"
-#include "rkv_launch.h"
+// fn batched_multihead_attention_optimized, and trustformers-core 0.2.0
+// src/gpu_ops/cuda/oxicuda/attention.rs, fn attention_prefill_gpu_to_gpu.
+#include "prefill_tc.cuh"
 
 namespace rkv {
 
-constexpr int kPfBM = 128;                    // query rows per CTA (TMEM lanes)
-constexpr int kPfThreads = 384;               // 12 warps
-constexpr int kPfPvWarp = 10;                 // PV issuer
-constexpr int kPfVWarp0 = 6;                  // first V transposer warp
-constexpr int kPfVProdWarp = 11;              // V producer and output stores
-constexpr uint32_t kPfTmemCols = 512;
-constexpr uint32_t kColQ = 0, kColO = 128, kColS = 256;   // TMEM column bases
-constexpr float kPfLog2e = 1.4426950408889634f;
-constexpr float kLazyRescale = 8.0f;          // log2 of the largest unnormalised p kept
-constexpr int kPfMinSmem = 120 * 1024;        // keeps one CTA per SM (TMEM is allocated whole)
-
-template <int D>
-struct PfCfg {
-    static constexpr int BN = D == 128 ? 64 : 128;          // keys per block
-    static constexpr int CH = D >= 32 ? 32 : D;             // floats per swizzled K row chunk
-    static constexpr int NCH = D / CH;
-    static constexpr int TILE = BN * D * 4;                 // bytes of one K or V^T tile
-    // D = 128: K slots come in adjacent pairs so one N = 128 MMA chain computes the scores
-    // of two 64-key blocks (half the MMAs of N = 64; a thread needs ~45+ cycles per issue).
-    static constexpr bool KPAIR = D == 128;
-    static constexpr int NK = KPAIR ? 4 : (D >= 64 ? 3 : 4);   // K stages
-    static constexpr int NV = D >= 64 ? 3 : 4;              // V^T stages
-    // S/P buffers in TMEM: the MMA issuer runs up to NSBUF blocks of QK^T ahead of the
-    // softmax, so the tensor core always has queued work.  D <= 64: PV is split over
-    // even/odd key steps into two accumulators (O = O_a + O_b).
-    static constexpr int NSBUF = D == 128 ? 4 : 2;
-    static constexpr int PV_SPLIT = D <= 64 ? 2 : 1;
-    static constexpr int S_BUF = BN;                       // TMEM columns of one S buffer
-    static constexpr uint32_t K_SWIZZLE = D >= 32 ? kSwizzle128B : kSwizzle64B;
-    static constexpr uint32_t K_ATOM = D >= 32 ? 1024 : 512; // 8 rows x swizzle span
-    // Each item's query tile travels through the K ring ahead of its K tiles, as QSLOTS
-    // fills of BN rows (same box as a K tile).  With paired slots the query fills take one
-    // aligned slot pair, so their 128 rows sit at a uniform stride like an MMA operand.
-    static constexpr int QSLOTS = kPfBM / BN;
-    static_assert(QSLOTS <= NK && (!KPAIR || QSLOTS == 2), "query fills in the K ring");
-    // Each item's output tile (kPfBM x D) is staged in OSLOTS V-ring slots, each holding
-    // OCH column chunks of CH floats for all kPfBM rows (swizzled like the TMA box).
-    static constexpr int OSLOTS = kPfBM / BN;
-    static constexpr int OCH = NCH / OSLOTS;
-    static_assert(OSLOTS < NV && OSLOTS * OCH == NCH && OCH * kPfBM * CH * 4 == TILE, "output staging");
-    // shared memory layout (offsets from a 1024-aligned base)
-    static constexpr int OFF_K = 0;
-    // byte offset of d-chunk c of K slot s: paired slots interleave their chunks so the
-    // 2*BN rows of a chunk are contiguous (uniform 1024-byte stride per 8 rows)
-    __host__ __device__ static constexpr int koff(int s, int c) {
-        return KPAIR ? (s / 2) * 2 * TILE + c * (2 * BN * CH * 4) + (s % 2) * (BN * CH * 4)
-                     : s * TILE + c * (BN * CH * 4);
-    }
-    static constexpr int OFF_V = OFF_K + NK * TILE;
-    static constexpr int OFF_BAR = OFF_V + NV * TILE;
-    // barriers: k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], v_loaded[NV], s_full[NSBUF],
-    //           p_ready[NSBUF], o_done[NSBUF], o_final, q_free, o_free, drain, drain_pv
-    static constexpr int NBAR = 2 * NK + 3 * NV + 3 * NSBUF + 5;
-    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;     // tmem base, abort flag
-    static constexpr int SMEM_USED = OFF_MISC + 16;
-    static constexpr int SMEM = (SMEM_USED + 1024 > kPfMinSmem ? SMEM_USED + 1024 : kPfMinSmem);
-    static_assert(SMEM <= 227 * 1024, "prefill shared memory budget");
-    static_assert(kColS + NSBUF * S_BUF <= (int)kPfTmemCols && kColO + PV_SPLIT * D <= kColS && D <= 128,
-                  "TMEM budget");
-};
-
-struct PfBars {
-    uint32_t k_full, k_empty, v_full, v_empty, v_loaded, s_full, p_ready, o_done, o_final, q_free, o_free,
-        drain, drain_pv;
-};
-
-template <int NK, int NV, int NSB>
-__device__ __forceinline__ PfBars pf_bars(uint32_t base) {
-    PfBars b;
-    b.k_full = base;
-    b.k_empty = b.k_full + 8 * NK;
-    b.v_full = b.k_empty + 8 * NK;
-    b.v_empty = b.v_full + 8 * NV;
-    b.v_loaded = b.v_empty + 8 * NV;
-    b.s_full = b.v_loaded + 8 * NV;
-    b.p_ready = b.s_full + 8 * NSB;
-    b.o_done = b.p_ready + 8 * NSB;
-    b.o_final = b.o_done + 8 * NSB;
-    b.q_free = b.o_final + 8;
-    b.o_free = b.q_free + 8;
-    b.drain = b.o_free + 8;
-    b.drain_pv = b.drain + 8;
-    return b;
-}
-
-// One work item: a 128-query tile of one (batch, head).
-struct PfWork {
-    int b, h, g, q0, len, nblk;
-};
-
-// Work items are numbered heaviest causal tiles first: u -> (tile n_qtiles-1-u/BH, bh = u%BH).
-template <int D>
-__device__ __forceinline__ PfWork pf_work(int u, int B, int H, int Hk, int S, int n_qtiles, int causal,
-                                          const int* __restrict__ seq_lens) {
-    const int BH = B * H;
-    PfWork w;
-    const int tile = n_qtiles - 1 - u / BH;
-    const int bh = u % BH;
-    w.b = bh / H;
-    w.h = bh % H;
-    w.g = w.h / (H / Hk);
-    w.q0 = tile * kPfBM;
-    w.len = seq_lens ? min(max(__ldg(seq_lens + w.b), 0), S) : S;
-    const int kv_end = w.q0 >= w.len ? 0 : (causal ? min(w.len, w.q0 + kPfBM) : w.len);
-    w.nblk = (kv_end + PfCfg<D>::BN - 1) / PfCfg<D>::BN;
-    return w;
-}
-
-// The k-th work item of this CTA.  Items are dealt in rounds of gridDim.x, every other
-// round in reverse CTA order, so the heavy-first costs even out across CTAs.
-__device__ __forceinline__ int pf_item(int k) {
-    const int G = (int)gridDim.x;
-    return k * G + ((k & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
-}
-
-template <int D>
-__global__ void __launch_bounds__(kPfThreads, 1)
-prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
-                  float* __restrict__ o,
-                  int B, int S, int H, int Hk, int causal, const int* __restrict__ seq_lens, float scale_log2,
-                  int n_qtiles, int n_work, unsigned int* __restrict__ flags) {
-    using C = PfCfg<D>;
-    constexpr int BN = C::BN;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                           ~static_cast<uintptr_t>(1023));
-    const PfBars bar = pf_bars<C::NK, C::NV, C::NSBUF>(smem_addr(smem + C::OFF_BAR));
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t q_row = (int64_t)H * D;
-    auto work = [&](int u) { return pf_work<D>(u, B, H, Hk, S, n_qtiles, causal, seq_lens); };
-
-    if (seq_lens && blockIdx.x == 0) {     // report clamped lengths once per launch
-        for (int i = threadIdx.x; i < B; i += blockDim.x) {
-            const int l = __ldg(seq_lens + i);
-            if (l > S) atomicOr(flags, RKV_FLAG_LEN_CLAMPED);
-            if (l < 0) atomicOr(flags, RKV_FLAG_NEGATIVE_INPUT);
-        }
-    }
-
-    // ------------------------------------------------------------------ setup
-    if (warp == 1) {
-        tmem_alloc(smem_addr(tmem_slot), kPfTmemCols);
-        tmem_relinquish();
-    }
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < C::NK; ++s) {
-            mbar_init(bar.k_full + 8 * s, 1);
-            mbar_init(bar.k_empty + 8 * s, 1);
-        }
-        for (int s = 0; s < C::NV; ++s) {
-            mbar_init(bar.v_full + 8 * s, 128);
-            mbar_init(bar.v_empty + 8 * s, 1);
-            mbar_init(bar.v_loaded + 8 * s, 1);
-        }
-        for (int s = 0; s < C::NSBUF; ++s) {
-            mbar_init(bar.s_full + 8 * s, 1);
-            mbar_init(bar.p_ready + 8 * s, 128);
-            mbar_init(bar.o_done + 8 * s, 1);
-        }
-        mbar_init(bar.o_final, 1);
-        mbar_init(bar.q_free, 1);
-        mbar_init(bar.o_free, 128);
-        mbar_init(bar.drain, 1);
-        mbar_init(bar.drain_pv, 1);
-        *abort_flag = 0;
-        fence_barrier_init();
-        prefetch_tmap(&tm_k);
-        prefetch_tmap(&tm_v);
-        prefetch_tmap(&tm_q);
-        prefetch_tmap(&tm_o);
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-
-    // Every role walks the same item sequence and numbers key blocks with one running
-    // counter (g) across items, so ring slots and barrier phases continue from item to
-    // item.  Items without visible keys use no barrier at all.
-    if (warp == 0) {
-        // ================================================================ K producer
-        // lane 0: per item [pad] the query tile (QSLOTS fills) then one K tile per block, by TMA.
-        // With paired slots the query fills must start on an even fill; an empty pad fill (a
-        // plain arrival, no data) restores that after an odd block count.
-        if (lane == 0) {
-            int gs = 0;                   // fills of the K ring so far
-            bool ok = true;
-            for (int k = 0; ok; ++k) {
-                const int u = pf_item(k);
-                if (u >= n_work) break;
-                const PfWork w = work(u);
-                if (w.nblk == 0) continue;
-                {                   // the next item's query tile -> L2, ahead of its own copy
-                    const int un = pf_item(k + 1);
-                    if (un < n_work) {
-                        const PfWork wn = work(un);
-#pragma unroll
-                        for (int i = 0; i < C::QSLOTS; ++i)
-#pragma unroll
-                            for (int c = 0; c < C::NCH; ++c)
-                                tma_prefetch_l2_3d(&tm_q, wn.h * D + c * C::CH, wn.q0 + i * BN, wn.b);
-                    }
-                }
-                const bool pad = C::KPAIR && (gs & 1);
-                constexpr int nq = C::QSLOTS;
-                for (int j = -nq - (pad ? 1 : 0); j < w.nblk; ++j) {
-                    const int s = gs % C::NK;
-                    if (!(ok = mbar_wait(bar.k_empty + 8 * s, ((uint32_t)(gs / C::NK) & 1u) ^ 1u, abort_flag, flags)))
-                        break;
-                    const uint32_t full = bar.k_full + 8 * s;
-                    ++gs;
-                    if (j < -nq) {          // pad fill
-                        mbar_arrive(full);
-                        continue;
-                    }
-                    mbar_arrive_expect_tx(full, C::TILE);
-                    const bool qfill = j < 0;
-                    const void* map = qfill ? static_cast<const void*>(&tm_q) : static_cast<const void*>(&tm_k);
-                    const int x0 = (qfill ? w.h : w.g) * D;
-                    const int y0 = qfill ? w.q0 + (j + nq) * BN : j * BN;
-#pragma unroll
-                    for (int c = 0; c < C::NCH; ++c)
-                        tma_load_3d(smem_addr(smem + C::OFF_K) + C::koff(s, c), map, x0 + c * C::CH, y0, w.b, full);
-                }
-            }
-            if (*abort_flag) {   // unwinding: let issued copies land
-                for (int f = max(0, gs - C::NK); f < gs; ++f)
-                    mbar_drain(bar.k_full + 8 * (f % C::NK), (uint32_t)(f / C::NK) & 1u, 100000000ull);
-            }
-        }
-    } else if (warp == kPfVProdWarp) {
-        // ================================================================ V producer / O stores
-        // lane 0: per item one V tile per block by TMA, then OSLOTS output staging fills: no
-        // data, the slot is handed (plain arrival on v_loaded) to the epilogue, which writes
-        // O / l there and arrives on v_full.  This thread then stores the staged tile to the
-        // output by TMA and, once the copy engine has read it, releases the slots.  It does
-        // so before the first later fill that reuses one of them (or at the end).
-        if (lane == 0) {
-            int gs = 0;                   // fills of the V ring so far
-            bool ok = true;
-            int pend = -1;                // first staging fill not yet stored (-1: none)
-            PfWork pw{};                  // its item
-            auto flush = [&]() -> bool {
-                for (int i = 0; i < C::OSLOTS; ++i)
-                    if (!mbar_wait(bar.v_full + 8 * ((pend + i) % C::NV), (uint32_t)((pend + i) / C::NV) & 1u,
-                                   abort_flag, flags))
-                        return false;
-                for (int i = 0; i < C::OSLOTS; ++i) {
-                    const uint32_t src = smem_addr(smem + C::OFF_V) + ((pend + i) % C::NV) * C::TILE;
-#pragma unroll
-                    for (int cc = 0; cc < C::OCH; ++cc)
-                        tma_store_3d(&tm_o, src + cc * (kPfBM * C::CH * 4), pw.h * D + (i * C::OCH + cc) * C::CH,
-                                     pw.q0, pw.b);
-                }
-                bulk_commit();
-                bulk_wait_read_all();
-                for (int i = 0; i < C::OSLOTS; ++i) mbar_arrive(bar.v_empty + 8 * ((pend + i) % C::NV));
-                pend = -1;
-                return true;
-            };
-            for (int k = 0; ok; ++k) {
-                const int u = pf_item(k);
-                if (u >= n_work) break;
-                const PfWork w = work(u);
-                if (w.nblk == 0) continue;
-                for (int j = 0; j < w.nblk + C::OSLOTS; ++j) {
-                    if (pend >= 0 && gs >= pend + C::NV && !(ok = flush())) break;
-                    const int s = gs % C::NV;
-                    if (!(ok = mbar_wait(bar.v_empty + 8 * s, ((uint32_t)(gs / C::NV) & 1u) ^ 1u, abort_flag, flags)))
-                        break;
-                    const uint32_t full = bar.v_loaded + 8 * s;
-                    if (j >= w.nblk) {      // output staging fill
-                        if (j == w.nblk) { pend = gs; pw = w; }
-                        ++gs;
-                        mbar_arrive(full);
-                        continue;
-                    }
-                    ++gs;
-                    mbar_arrive_expect_tx(full, C::TILE);
-#pragma unroll
-                    for (int c = 0; c < C::NCH; ++c)
-                        tma_load_3d(smem_addr(smem + C::OFF_V) + s * C::TILE + c * BN * C::CH * 4, &tm_v,
-                                    w.g * D + c * C::CH, j * BN, w.b, full);
-                }
-            }
-            if (ok && pend >= 0) ok = flush();
-            bulk_wait_all();                  // output stores complete before the CTA exits
-            if (*abort_flag) {   // unwinding: let issued copies land
-                for (int f = max(0, gs - C::NV); f < gs; ++f)
-                    mbar_drain(bar.v_loaded + 8 * (f % C::NV), (uint32_t)(f / C::NV) & 1u, 100000000ull);
-            }
-        }
-    } else if (warp == 1 || warp == kPfPvWarp) {
-        // ================================================================ MMA issuers
-        // Two threads issue: warp 1 the QK^T MMAs, warp 10 the PV MMAs.  A thread needs
-        // ~45 cycles per tcgen05.mma it issues, more than one N=64 MMA takes to run,
-        // so a single issuer would starve the tensor core.
-        if (lane == 0) {
-            const bool qk_role = warp == 1;
-            constexpr uint32_t id_qk = idesc_tf32(kPfBM, BN, false);
-            constexpr uint32_t id_qk2 = idesc_tf32(kPfBM, 2 * BN, false);
-            constexpr uint32_t id_pv = idesc_tf32(kPfBM, D, false);
-            bool ok = true;
-            int issued_any = 0, g0 = 0, t = 0;   // t: items with keys so far
-            int f = 0;                           // K-ring fills consumed (QK^T issuer)
-            int fv = 0;                          // V-ring fills passed (PV issuer)
-            // Descriptors are built once; a k step or ring stage only adds its byte offset
-            // (>> 4) to the start-address field, which cannot carry out of it (shared
-            // addresses are below 2^18).
-            const uint64_t kdesc0 = smem_desc(smem_addr(smem + C::OFF_K), 16, C::K_ATOM, C::K_SWIZZLE);
-            const uint64_t vdesc0 = smem_desc(smem_addr(smem + C::OFF_V), 16, 1024, kSwizzle128B);
-            for (int k = 0; ok; ++k) {
-                const int u = pf_item(k);
-                if (u >= n_work) break;
-                const PfWork w = work(u);
-                if (w.nblk == 0) continue;
-                if (qk_role) {
-                    // K-ring fills of this item: [pad] query tile (QSLOTS) then one per key block
-                    if (C::KPAIR && (f & 1)) {      // pad fill: nothing to read, hand it back
-                        if (!(ok = mbar_wait(bar.k_full + 8 * (f % C::NK), (uint32_t)(f / C::NK) & 1u, abort_flag,
-                                             flags)))
-                            break;
-                        mbar_arrive(bar.k_empty + 8 * (f % C::NK));
-                        ++f;
-                    }
-                    // Q -> TMEM columns kColQ.. by tcgen05.cp, once the previous item's QK^T
-                    // MMAs (committed to q_free) are done reading them.  The copies run ahead
-                    // of this thread's later MMAs in issue order.
-                    if (t > 0) ok = mbar_wait(bar.q_free, (uint32_t)(t - 1) & 1u, abort_flag, flags);
-                    for (int i = 0; ok && i < C::QSLOTS; ++i)
-                        ok = mbar_wait(bar.k_full + 8 * ((f + i) % C::NK), (uint32_t)((f + i) / C::NK) & 1u, abort_flag,
-                                       flags);
-                    if (!ok) break;
-                    tc_fence_after();
-                    {
-                        const int sq = f % C::NK;    // even when paired: the query tile fills a slot pair
-#pragma unroll
-                        for (int kk8 = 0; kk8 < D / 8; ++kk8) {
-                            const int c = kk8 / (C::CH / 8), kk = kk8 % (C::CH / 8);
-                            tmem_cp_128x256b(tmem + kColQ + 8 * kk8,
-                                             kdesc0 + (uint64_t)((C::koff(sq, c) + kk * 32) >> 4));
-                        }
-                        for (int i = 0; i < C::QSLOTS; ++i) mma_commit(bar.k_empty + 8 * ((f + i) % C::NK));
-                        f += C::QSLOTS;
-                    }
-                    // S of block gb goes to buffer gb % NSBUF.  Paired blocks (D = 128: fill f
-                    // even, adjacent buffers) share one N = 2*BN chain.  Before QK overwrites a
-                    // buffer, the PV that read P from it (block gb - NSBUF) must have finished.
-                    // The wait is exact: PV_{gb-2*NSBUF} completed before QK_{gb-NSBUF} was
-                    // issued, and PV_gb cannot have started (it needs S_gb).
-                    for (int j = 0; ok && j < w.nblk;) {
-                        const int gb = g0 + j, fb = f + j;
-                        const int nb = (C::KPAIR && (fb & 1) == 0 && gb % C::NSBUF != C::NSBUF - 1 && j + 1 < w.nblk)
-                                           ? 2 : 1;
-                        for (int i = 0; ok && i < nb; ++i) {
-                            if (gb + i >= C::NSBUF)
-                                ok = mbar_wait(bar.o_done + 8 * ((gb + i) % C::NSBUF),
-                                               (uint32_t)((gb + i - C::NSBUF) / C::NSBUF) & 1u, abort_flag, flags);
-                            if (ok)
-                                ok = mbar_wait(bar.k_full + 8 * ((fb + i) % C::NK), (uint32_t)((fb + i) / C::NK) & 1u,
-                                               abort_flag, flags);
-                        }
-                        if (!ok) break;
-                        tc_fence_after();
-                        const int s = fb % C::NK;
-                        const uint32_t d_tmem = tmem + kColS + (uint32_t)((gb % C::NSBUF) * C::S_BUF);
-#pragma unroll
-                        for (int kk8 = 0; kk8 < D / 8; ++kk8) {
-                            const int c = kk8 / (C::CH / 8), kk = kk8 % (C::CH / 8);
-                            const uint64_t bdesc = kdesc0 + (uint64_t)((C::koff(s, c) + kk * 32) >> 4);
-                            mma_tf32_ts(d_tmem, tmem + kColQ + 8 * kk8, bdesc, nb == 2 ? id_qk2 : id_qk,
-                                        kk8 > 0 ? 1u : 0u);
-                        }
-                        for (int i = 0; i < nb; ++i) {
-                            mma_commit(bar.s_full + 8 * ((gb + i) % C::NSBUF));
-                            mma_commit(bar.k_empty + 8 * ((fb + i) % C::NK));
-                        }
-                        issued_any = 1;
-                        j += nb;
-                    }
-                    if (!ok) break;
-                    f += w.nblk;
-                    mma_commit(bar.q_free);    // all QK^T of this item done: Q columns reusable
-                } else {
-                    // O is reused item after item: PV of a new item starts (accumulate = 0)
-                    // only after the epilogue has read the previous item's O.
-                    if (t > 0) ok = mbar_wait(bar.o_free, (uint32_t)(t - 1) & 1u, abort_flag, flags);
-                    for (int j = 0; ok && j < w.nblk; ++j) {
-                        // O += P_gb V_gb
-                        const int gb = g0 + j, vf = fv + j;
-                        const int sv = vf % C::NV, sb = gb % C::NSBUF;
-                        if (!(ok = mbar_wait(bar.p_ready + 8 * sb, (uint32_t)(gb / C::NSBUF) & 1u, abort_flag, flags)))
-                            break;
-                        if (!(ok = mbar_wait(bar.v_full + 8 * sv, (uint32_t)(vf / C::NV) & 1u, abort_flag, flags)))
-                            break;
-                        tc_fence_after();
-                        const uint64_t vd = vdesc0 + (uint64_t)(sv * (C::TILE >> 4));
-                        const uint32_t a_tmem = tmem + kColS + (uint32_t)(sb * C::S_BUF);
-                        const uint32_t first = j > 0 ? 1u : 0u;
-#pragma unroll
-                        for (int kk8 = 0; kk8 < BN / 8; ++kk8) {
-                            // V^T tile: rows = d, 32 keys per 128-byte row, key chunks D*128 bytes apart
-                            const uint64_t bdesc = vd + (uint64_t)(((kk8 / 4) * (D * 128) + (kk8 % 4) * 32) >> 4);
-                            const int part = kk8 % C::PV_SPLIT;
-                            mma_tf32_ts(tmem + kColO + part * D, a_tmem + 8 * kk8, bdesc, id_pv,
-                                        kk8 >= C::PV_SPLIT ? 1u : first);
-                        }
-                        mma_commit(bar.o_done + 8 * sb);
-                        mma_commit(bar.v_empty + 8 * sv);
-                        issued_any = 1;
-                    }
-                    if (!ok) break;
-                    mma_commit(bar.o_final);
-                    fv += w.nblk + C::OSLOTS;          // the item's V tiles and output staging fills
-                }
-                g0 += w.nblk;
-                ++t;
-            }
-            if (!ok && issued_any) {   // unwinding: let issued MMAs finish before TMEM is freed
-                const uint32_t dr = qk_role ? bar.drain : bar.drain_pv;
-                mma_commit(dr);
-                mbar_drain(dr, 0, 100000000ull);
-            }
-        }
-    } else if (warp >= kPfVWarp0 && warp < kPfVWarp0 + 4) {
-        // ================================================================ V transposer
-        // V tiles arrive by TMA in the same swizzled layout as K (rows = keys).  The
-        // transposer rewrites each slot in place as V^T: work item = (key quad aa,
-        // d quad dq), a 4x4 block read with four 16-byte loads and written as four
-        // 16-byte rows of V^T.  Lane numbering puts 4 consecutive key quads x 2 d
-        // quads (D = 16: 8 key quads x 1) in each quarter-warp, so its eight V^T
-        // stores hit eight distinct 128-byte-swizzle chunks: no conflicts.
-        const int wv = warp - kPfVWarp0;                      // 0..3
-        constexpr int LDQ = D / 4 < 8 ? D / 4 : 8;           // lanes along d quads
-        constexpr int LAA = 32 / LDQ;                        // lanes along key quads
-        constexpr int GA = (BN / 4) / LAA;                   // lane groups along keys
-        constexpr int GD = (D / 4) / LDQ;                    // lane groups along d
-        constexpr int PER = GA * GD / 4;                     // groups per warp
-        static_assert(GA * GD % 4 == 0 && PER >= 1, "V transposer work split");
-        const int aa_lo = lane % LAA, dq_lo = lane / LAA;
-        // Byte offset of V[key][d] in a TMA-staged tile (box {CH floats, BN keys} per
-        // d chunk, swizzled: 16-byte chunk index XOR key bits).
-        auto staged = [](int key, int dq) -> int {
-            if constexpr (D >= 32)
-                return (dq >> 3) * (BN * 128) + key * 128 + (((dq & 7) ^ (key & 7)) << 4);
-            else
-                return key * 64 + (((dq & 3) ^ ((key >> 1) & 3)) << 4);
-        };
-        bool ok = true;
-        int gb = 0;                                          // V-ring fills passed
-        for (int k = 0; ok; ++k) {
-            const int u = pf_item(k);
-            if (u >= n_work) break;
-            const PfWork w = work(u);
-            if (w.nblk == 0) continue;
-            // ---- V tiles of this item
-            for (int j = 0; j < w.nblk; ++j, ++gb) {
-                const int s = gb % C::NV;
-                unsigned char* vt = smem + C::OFF_V + s * C::TILE;
-                const bool loaded = mbar_wait(bar.v_loaded + 8 * s, (uint32_t)(gb / C::NV) & 1u, abort_flag, flags);
-                float4 x[PER][4];
-#pragma unroll
-                for (int it = 0; it < PER && loaded; ++it) {
-                    const int G = it * 4 + wv;
-                    const int aa = (G % GA) * LAA + aa_lo;
-                    const int dq = (G / GA) * LDQ + dq_lo;
-#pragma unroll
-                    for (int rr = 0; rr < 4; ++rr) {
-                        const int key = aa * 4 + rr;
-                        // keys past the sequence end were zero-filled by the copy engine
-                        x[it][rr] = *reinterpret_cast<const float4*>(vt + staged(key, dq));
-                    }
-                }
-                // every thread has read its blocks: rewrite in place (or leave, all together)
-                if (named_barrier_or(2, 128, !loaded || *abort_flag)) { ok = false; break; }
-#pragma unroll
-                for (int it = 0; it < PER; ++it) {
-                    const int G = it * 4 + wv;
-                    const int aa = (G % GA) * LAA + aa_lo;
-                    const int dq = (G / GA) * LDQ + dq_lo;
-                    const int kc = aa >> 3;                      // 32-key chunk of the V^T row
-                    const float4 c0 = x[it][0], c1 = x[it][1], c2 = x[it][2], c3 = x[it][3];
-                    const uint4 wr[4] = {
-                        make_uint4(__float_as_uint(c0.x), __float_as_uint(c1.x), __float_as_uint(c2.x), __float_as_uint(c3.x)),
-                        make_uint4(__float_as_uint(c0.y), __float_as_uint(c1.y), __float_as_uint(c2.y), __float_as_uint(c3.y)),
-                        make_uint4(__float_as_uint(c0.z), __float_as_uint(c1.z), __float_as_uint(c2.z), __float_as_uint(c3.z)),
-                        make_uint4(__float_as_uint(c0.w), __float_as_uint(c1.w), __float_as_uint(c2.w), __float_as_uint(c3.w))};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int d = dq * 4 + i;
-                        const int off = kc * (D * 128) + d * 128 + (((aa & 7) ^ (d & 7)) << 4);
-                        *reinterpret_cast<uint4*>(vt + off) = wr[i];
-                    }
-                }
-                fence_proxy_async();          // generic-proxy stores -> tensor-core reads
-                mbar_arrive(bar.v_full + 8 * s);
-            }
-            gb += C::OSLOTS;                                 // output staging fills: the epilogue's
-        }
-    } else {
-        // ================================================================ softmax / epilogue
-        const int quad = warp & 3;                       // TMEM lane quadrant of this warp
-        const int r = quad * 32 + lane;                  // query row within the tile
-        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        bool ok = true;
-        int g0 = 0, t = 0, fv = 0;     // blocks, items with keys, V-ring fills passed
-        for (int k = 0; ok; ++k) {
-            const int u = pf_item(k);
-            if (u >= n_work) break;
-            const PfWork w = work(u);
-            const int qi = w.q0 + r;
-            float4* op = reinterpret_cast<float4*>(o + ((int64_t)w.b * S + qi) * q_row + (int64_t)w.h * D);
-            if (w.nblk == 0) {      // no key is visible to any row of this tile: padding -> zeros
-                if (qi < S) {
-#pragma unroll
-                    for (int e = 0; e < D / 4; ++e) __stcs(op + e, make_float4(0.f, 0.f, 0.f, 0.f));
-                }
-                continue;
-            }
-            float m_run = -INFINITY, l_run = 0.0f;
-            const int key_lim = causal ? min(qi + 1, w.len) : w.len;   // keys visible to this row
-            for (int j = 0; j < w.nblk; ++j) {
-                const int gb = g0 + j;
-                ok = mbar_wait(bar.s_full + 8 * (gb % C::NSBUF), (uint32_t)(gb / C::NSBUF) & 1u, abort_flag, flags);
-                if (!(ok = __all_sync(0xffffffffu, ok))) break;   // warp-uniform before TMEM access
-                tc_fence_after();
-                const uint32_t s_col = lane_base + kColS + (uint32_t)((gb % C::NSBUF) * C::S_BUF);
-                float s[BN];
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t wv[32];
-                    tmem_ld32(s_col + 32 * c, wv);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(wv[e]);
-                }
-                const int k0 = j * BN;
-                const int nvis = min(max(key_lim - k0, 0), BN);     // visible keys of this block
-                if (__any_sync(0xffffffffu, nvis < BN)) {
-#pragma unroll
-                    for (int e = 0; e < BN; ++e)
-                        if (e >= nvis) s[e] = -INFINITY;
-                }
-                float mx[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) mx[e] = s[e];
-#pragma unroll
-                for (int e = 8; e < BN; ++e) mx[e & 7] = fmaxf(mx[e & 7], s[e]);
-                // S holds raw q.k; scores in the exponent's units are s * scale*log2(e) (> 0,
-                // so the maximum commutes with the scaling)
-                const float m_blk = scale_log2 * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-                // m_use is finite: every row of an item with keys sees at least key 0
-                const bool need = m_blk > m_run + kLazyRescale;
-                const float m_use = need ? m_blk : m_run;
-                const float alpha = need ? fast_exp2(m_run - m_blk) : 1.0f;
-                // p = 2^(s*c - m); the tensor core truncates f32 operands to TF32, so p is
-                // truncated here too and the row sum is taken over exactly those values
-                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t wv[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float x = s[32 * c + e];
-                        const float p = fast_exp2(fmaf(x, scale_log2, -m_use));   // 2^-inf = +0 when masked
-                        wv[e] = __float_as_uint(p) & 0xFFFFE000u;
-                        ls[e & 7] += __uint_as_float(wv[e]);
-                    }
-                    tmem_st32(s_col + 32 * c, wv);
-                }
-                const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-                l_run = l_run * alpha + lsum;
-                m_run = m_use;
-                tmem_wait_st();
-                if (j > 0 && __any_sync(0xffffffffu, need)) {
-                    // O holds blocks < j once PV_{gb-1} completes; scale it by alpha.  Seeing S_gb
-                    // means PV_{gb-NSBUF} completed (issued before QK_gb), so the barrier of
-                    // PV_{gb-1}'s buffer is at most one phase behind: the parity wait is exact.
-                    ok = mbar_wait(bar.o_done + 8 * ((gb - 1) % C::NSBUF), (uint32_t)((gb - 1) / C::NSBUF) & 1u,
-                                   abort_flag, flags);
-                    if (!(ok = __all_sync(0xffffffffu, ok))) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int c = 0; c < C::PV_SPLIT * ((D + 31) / 32); ++c) {
-                        if constexpr (D >= 32) {
-                            uint32_t wv[32];
-                            tmem_ld32(lane_base + kColO + 32 * c, wv);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) wv[e] = __float_as_uint(__uint_as_float(wv[e]) * alpha);
-                            tmem_st32(lane_base + kColO + 32 * c, wv);
-                        } else {
-                            uint32_t wv[16];
-                            tmem_ld16(lane_base + kColO + 16 * c, wv);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) wv[e] = __float_as_uint(__uint_as_float(wv[e]) * alpha);
-                            tmem_st16(lane_base + kColO + 16 * c, wv);
-                        }
-                    }
-                    tmem_wait_st();
-                }
-                tc_fence_before();
-                mbar_arrive(bar.p_ready + 8 * (gb % C::NSBUF));
-            }
-            if (!ok) break;
-            // ---------------------------------------------------------- epilogue
-            // O / l goes to the item's output staging fills (after its V tiles in the V
-            // ring); the V producer stores them to the output by TMA.
-            ok = mbar_wait(bar.o_final, (uint32_t)t & 1u, abort_flag, flags);
-            if (!(ok = __all_sync(0xffffffffu, ok))) break;
-            tc_fence_after();
-            const float inv = (qi < w.len && l_run > 0.0f) ? 1.0f / l_run : 0.0f;
-            const int fs = fv + w.nblk;                          // first staging fill
-#pragma unroll 1
-            for (int i = 0; ok && i < C::OSLOTS; ++i) {
-                ok = mbar_wait(bar.v_loaded + 8 * ((fs + i) % C::NV), (uint32_t)((fs + i) / C::NV) & 1u, abort_flag,
-                               flags);
-                if (!(ok = __all_sync(0xffffffffu, ok))) break;
-                unsigned char* stage = smem + C::OFF_V + ((fs + i) % C::NV) * C::TILE;
-#pragma unroll
-                for (int cc = 0; cc < C::OCH; ++cc) {
-                    const int c = i * C::OCH + cc;               // column chunk of O
-                    unsigned char* dst = stage + cc * (kPfBM * C::CH * 4);
-                    if constexpr (C::CH == 32) {
-                        uint32_t wv[32];
-                        tmem_ld32(lane_base + kColO + 32 * c, wv);
-                        if constexpr (C::PV_SPLIT == 2) {            // O = O_a + O_b
-                            uint32_t w2[32];
-                            tmem_ld32(lane_base + kColO + D + 32 * c, w2);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                wv[e] = __float_as_uint(__uint_as_float(wv[e]) + __uint_as_float(w2[e]));
-                        } else {
-                            tmem_wait_ld();
-                        }
-                        // 128-byte rows, 16-byte chunk index XOR row bits (the TMA box swizzle)
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            *reinterpret_cast<float4*>(dst + r * 128 + (((e & 7) ^ (r & 7)) << 4)) =
-                                make_float4(__uint_as_float(wv[4 * e]) * inv, __uint_as_float(wv[4 * e + 1]) * inv,
-                                            __uint_as_float(wv[4 * e + 2]) * inv, __uint_as_float(wv[4 * e + 3]) * inv);
-                    } else {
-                        uint32_t wv[16], w2[16];
-                        tmem_ld16(lane_base + kColO, wv);
-                        tmem_ld16(lane_base + kColO + D, w2);      // D = 16 always splits PV
-                        tmem_wait_ld();
-                        // 64-byte rows, 64-byte swizzle
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            *reinterpret_cast<float4*>(dst + r * 64 + (((e & 3) ^ ((r >> 1) & 3)) << 4)) = make_float4(
-                                (__uint_as_float(wv[4 * e]) + __uint_as_float(w2[4 * e])) * inv,
-                                (__uint_as_float(wv[4 * e + 1]) + __uint_as_float(w2[4 * e + 1])) * inv,
-                                (__uint_as_float(wv[4 * e + 2]) + __uint_as_float(w2[4 * e + 2])) * inv,
-                                (__uint_as_float(wv[4 * e + 3]) + __uint_as_float(w2[4 * e + 3])) * inv);
-                    }
-                }
-                fence_proxy_async();                             // generic stores -> TMA reads
-                mbar_arrive(bar.v_full + 8 * ((fs + i) % C::NV));
-            }
-            if (!ok) break;
-            fv += w.nblk + C::OSLOTS;
-            tc_fence_before();
-            mbar_arrive(bar.o_free);     // O may be overwritten by the next item's first PV
-            g0 += w.nblk;
-            ++t;
-        }
-    }
-
-    // ---------------------------------------------------------------- teardown
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, kPfTmemCols);
-    }
-}
-
-// ------------------------------------------------------------------ host side
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult qr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
-                cudaSuccess &&
-            qr == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-template <int D>
-static rkv_status launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
-    using C = PfCfg<D>;
-    auto encode = tensor_map_encoder();
-    if (!encode) return set_error(RKV_ERR_LAUNCH, "attn_prefill: cuTensorMapEncodeTiled unavailable");
-    CUtensorMap tm_k, tm_v, tm_q, tm_o;
-    const cuuint64_t dims[3] = {(cuuint64_t)a.Hk * D, (cuuint64_t)a.S, (cuuint64_t)a.B};
-    const cuuint64_t strides[2] = {(cuuint64_t)a.Hk * D * 4, (cuuint64_t)a.S * a.Hk * D * 4};
-    const cuuint32_t box[3] = {(cuuint32_t)C::CH, (cuuint32_t)C::BN, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    const CUtensorMapSwizzle sw = D >= 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    CUresult cr = encode(&tm_k, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(a.k), dims, strides, box,
-                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr == CUDA_SUCCESS)
-        cr = encode(&tm_v, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(a.v), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr == CUDA_SUCCESS) {
-        const cuuint64_t qdims[3] = {(cuuint64_t)a.H * D, (cuuint64_t)a.S, (cuuint64_t)a.B};
-        const cuuint64_t qstrides[2] = {(cuuint64_t)a.H * D * 4, (cuuint64_t)a.S * a.H * D * 4};
-        const cuuint32_t qbox[3] = {(cuuint32_t)C::CH, (cuuint32_t)C::BN, 1};   // one query fill
-        cr = encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(a.q), qdims, qstrides, qbox, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        // output: same shape as the query; one staged column chunk of a whole tile per store
-        // (rows past the sequence end are clipped by the copy engine)
-        const cuuint32_t obox[3] = {(cuuint32_t)C::CH, (cuuint32_t)kPfBM, 1};
-        if (cr == CUDA_SUCCESS)
-            cr = encode(&tm_o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.o, qdims, qstrides, obox, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    }
-    if (cr != CUDA_SUCCESS) return set_error(RKV_ERR_LAUNCH, "attn_prefill: tensor map encode failed (%d)", (int)cr);
-    auto kern = prefill_tc_kernel<D>;
-    static bool attr_done[64] = {false};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-            return check_launch("attn_prefill: shared-memory attribute");
-        attr_done[dev] = true;
-    }
-    const int n_qtiles = (a.S + kPfBM - 1) / kPfBM;
-    const int64_t n_work = (int64_t)n_qtiles * a.B * a.H;
-    if (n_work > (int64_t)1 << 30) return set_error(RKV_ERR_UNSUPPORTED, "attn_prefill: too many query tiles");
-    // persistent: one CTA per SM (at most one per work item)
-    const int sms = sm_count();
-    if (sms <= 0) return set_error(RKV_ERR_LAUNCH, "attn_prefill: cannot query the SM count");
-    const int grid = (int)(n_work < (int64_t)sms ? n_work : (int64_t)sms);
-    kern<<<grid, kPfThreads, C::SMEM, stream>>>(tm_k, tm_v, tm_q, tm_o, a.o, a.B, a.S, a.H, a.Hk, a.causal ? 1 : 0,
-                                                a.seq_lens, a.scale * kPfLog2e, n_qtiles, (int)n_work, a.flags);
-    return check_launch("attn_prefill");
-}
+rkv_status launch_prefill_guarded(const PrefillArgs& a, cudaStream_t stream);   // prefill_tc_guarded.cu
 
 rkv_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+    // per-sequence lengths or keys from the cache: tiles may reach past a sequence
+    if (a.kv_cache || a.seq_lens) return launch_prefill_guarded(a, stream);
     switch (a.D) {
-        case 16: return launch_prefill_tc_t<16>(a, stream);
-        case 32: return launch_prefill_tc_t<32>(a, stream);
-        case 64: return launch_prefill_tc_t<64>(a, stream);
-        case 128: return launch_prefill_tc_t<128>(a, stream);
+        case 16: return launch_prefill_tc_t<16, false>(a, stream);
+        case 32: return launch_prefill_tc_t<32, false>(a, stream);
+        case 64: return launch_prefill_tc_t<64, false>(a, stream);
+        case 128: return launch_prefill_tc_t<128, false>(a, stream);
     }
-    return set_error(RKV_ERR_UNSUPPORTED, "attn_prefill: head_dim %d", a.D);
+    return set_error(RKV_ERR_UNSUPPORTED, "%s: head_dim %d", a.op, a.D);
 }
 
 }  // namespace rkv

@@ -162,7 +162,41 @@ rkv_status attn_prefill(const float* q, const float* k, const float* v, float* o
     if ((const void*)o == (const void*)q || (const void*)o == (const void*)k || (const void*)o == (const void*)v)
         return set_error(RKV_ERR_INVALID_ARG, "%s: o must not alias q, k or v", op);
     PrefillArgs a{q, k, v, o, batch, seq_len, n_heads, n_kv_heads, head_dim, causal != 0, seq_lens, sc,
-                  device_flags_ptr()};
+                  device_flags_ptr(), op, false, 0, nullptr};
+    if (!a.flags) return set_error(RKV_ERR_LAUNCH, "%s: device flag word unavailable", op);
+    return launch_prefill(a, stream);
+}
+
+rkv_status attn_prefill_chunked(const float* q, const float* k_cache, const float* v_cache, float* o, int M,
+                                int T, int n_heads, int n_kv_heads, int head_dim, int max_len, int causal,
+                                const int* start_pos, const int* q_lens, float scale, cudaStream_t stream) {
+    const char* op = "attn_prefill_chunked";
+    g_msg[0] = 0;
+    if (M < 0 || M > kDecodeMaxSeqs)
+        return set_error(RKV_ERR_INVALID_ARG, "%s: M must be in [0, %d], got %d", op, kDecodeMaxSeqs, M);
+    if (T < 0) return set_error(RKV_ERR_INVALID_ARG, "%s: T must be >= 0, got %d", op, T);
+    rkv_status st = check_heads(n_heads, n_kv_heads, head_dim, op);
+    if (st != RKV_OK) return st;
+    if (max_len <= 0) return set_error(RKV_ERR_INVALID_ARG, "%s: max_len must be > 0, got %d", op, max_len);
+    if (T > max_len) return set_error(RKV_ERR_INVALID_ARG, "%s: T (%d) exceeds max_len (%d)", op, T, max_len);
+    float sc;
+    if ((st = resolve_scale(scale, head_dim, sc, op)) != RKV_OK) return st;
+    if (M == 0 || T == 0) return RKV_OK;
+    if (!q || !k_cache || !v_cache || !o || !start_pos)
+        return set_error(RKV_ERR_INVALID_ARG, "%s: q, caches, o and start_pos must be non-NULL", op);
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) ||
+        !aligned(start_pos, 4) || !aligned(q_lens, 4))
+        return set_error(RKV_ERR_INVALID_ARG, "%s: q, caches and o must be 16-byte aligned", op);
+    int64_t nq, nc;
+    if (!elems(nq, {M, T, n_heads, head_dim}) || !elems(nc, {M, n_kv_heads, max_len, head_dim}))
+        return set_error(RKV_ERR_INVALID_ARG, "%s: tensor sizes overflow int64", op);
+    if ((int64_t)max_len * head_dim * 4 >= (int64_t(1) << 40))
+        return set_error(RKV_ERR_UNSUPPORTED, "%s: cache stride beyond the kernel's limits", op);
+    if ((const void*)o == (const void*)q || (const void*)o == (const void*)k_cache ||
+        (const void*)o == (const void*)v_cache)
+        return set_error(RKV_ERR_INVALID_ARG, "%s: o must not alias q or the caches", op);
+    PrefillArgs a{q, k_cache, v_cache, o, M, T, n_heads, n_kv_heads, head_dim, causal != 0, q_lens, sc,
+                  device_flags_ptr(), op, true, max_len, start_pos};
     if (!a.flags) return set_error(RKV_ERR_LAUNCH, "%s: device flag word unavailable", op);
     return launch_prefill(a, stream);
 }

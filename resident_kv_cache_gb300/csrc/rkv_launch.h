@@ -13,14 +13,18 @@ constexpr int kDecodeMaxSeqs = 32;
 
 struct PrefillArgs {
     const float* q;
-    const float* k;
+    const float* k;        // interleaved [B, S, Hk*D], or the cache [B, Hk, max_len, D] (kv_cache)
     const float* v;
     float* o;
     int B, S, H, Hk, D;
     bool causal;
-    const int* seq_lens;   // device, may be NULL
+    const int* seq_lens;   // device valid query rows, may be NULL
     float scale;           // resolved (never 0)
     unsigned int* flags;   // device flag word
+    const char* op;        // entry point name for messages
+    bool kv_cache;         // K/V read from the cache: query i sits at key position start_pos + i
+    int max_len;           // cache capacity (kv_cache)
+    const int* start_pos;  // device int32[B] (kv_cache)
 };
 
 struct DecodeArgs {

@@ -22,7 +22,7 @@ def lib():
 
 def test_library_exports_every_declared_function(lib):
     names = binding.declared_functions()
-    assert set(names) >= {"attn_prefill", "attn_decode_batched", "attn_decode_workspace_bytes",
+    assert set(names) >= {"attn_prefill", "attn_prefill_chunked", "attn_decode_batched", "attn_decode_workspace_bytes",
                           "kv_cache_scatter", "rkv_last_error", "rkv_status_string",
                           "rkv_read_device_flags", "rkv_version"}
     for n in names:
@@ -109,6 +109,26 @@ def test_decode_workspace_query(lib):
 ])
 def test_scatter_host_validation(lib, args, status):
     _expect(status, binding.kv_cache_scatter, *args, stream=0)
+
+
+@pytest.mark.parametrize("args,status", [
+    ((A, A, A, 2 * A, 33, 8, 4, 2, 64, 128, 1, A), INV),       # M > 32 (batched cache limit)
+    ((A, A, A, 2 * A, 2, 200, 4, 2, 64, 128, 1, A), INV),      # T > max_len
+    ((A, A, A, 2 * A, 2, 8, 4, 2, 64, 0, 1, A), INV),          # max_len 0
+    ((A, A, A, 2 * A, 2, 8, 6, 4, 64, 128, 1, A), INV),        # n_heads % n_kv_heads
+    ((A, A, A, 2 * A, 2, 8, 4, 2, 96, 128, 1, A), UNS),        # head_dim
+    ((A, A, A, 2 * A, 2, 8, 4, 2, 64, 128, 1, None), INV),     # start_pos NULL
+    ((A, A + 4, A, 2 * A, 2, 8, 4, 2, 64, 128, 1, A), INV),    # misaligned cache
+    ((A, A, A, A, 2, 8, 4, 2, 64, 128, 1, A), INV),            # o aliases q
+    ((A, A, A, 2 * A, 2, -1, 4, 2, 64, 128, 1, A), INV),       # negative T
+])
+def test_prefill_chunked_host_validation(lib, args, status):
+    _expect(status, binding.attn_prefill_chunked, *args, stream=0)
+
+
+def test_prefill_chunked_zero_sized_is_a_noop(lib):
+    binding.attn_prefill_chunked(None, None, None, None, 0, 8, 4, 2, 64, 128, 1, None, stream=0)
+    binding.attn_prefill_chunked(None, None, None, None, 3, 0, 4, 2, 64, 128, 1, None, stream=0)
 
 
 def test_last_error_is_per_call(lib):
