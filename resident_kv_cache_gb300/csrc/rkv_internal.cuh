@@ -68,13 +68,6 @@ __device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t nthreads,
     return r != 0;
 }
 
-// x rounded toward +infinity to its upper 16 bits (a bfloat16 pattern, low bits zero); NaN
-// stays NaN, -inf stays -inf.
-__device__ __forceinline__ uint32_t round_up_16(float x) {
-    const uint32_t b = __float_as_uint(x);
-    return (b & 0x80000000u) ? (b & 0xFFFF0000u) : ((b + 0xFFFFu) & 0xFFFF0000u);
-}
-
 // Named barrier over `nthreads` threads (id 0 is __syncthreads).
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -160,3 +160,41 @@ def test_long_context_decode_sampled_steps(rkv, oracle_mod):
         assert_close(got, want, TOL, what=f"step {t}")
     hk, hv, _ = oracle_mod.scatter(kn_all, vn_all, k0, v0, 1, 256, Hk, D, L, start)
     assert np.array_equal(kc.cpu().numpy(), hk) and np.array_equal(vc.cpu().numpy(), hv)
+
+
+def test_append_and_decode_steps_replay_from_a_cuda_graph(rkv):
+    """Scatter + decode launches captured in a CUDA graph replay to the same bits as the
+    eager launches (the library never syncs, allocates or reads the host inside a call)."""
+    torch = torch_cuda()
+    M, H, Hk, D, L, steps = 2, 32, 8, 128, 1024, 8
+    kc0 = torch.from_numpy(inputs.normal((M, Hk, L, D), 501)).cuda()
+    vc0 = torch.from_numpy(inputs.normal((M, Hk, L, D), 502)).cuda()
+    qs = torch.from_numpy(inputs.normal((steps, M, H * D), 503)).cuda()
+    kn = torch.from_numpy(inputs.normal((steps, M, 1, Hk * D), 504)).cuda()
+    vn = torch.from_numpy(inputs.normal((steps, M, 1, Hk * D), 505)).cuda()
+    pos = torch.tensor([[500 + t, 900 + t] for t in range(steps)], dtype=torch.int32, device="cuda")
+    n = rkv.attn_decode_workspace_bytes(M, H, Hk, D, L)
+
+    def run(kc, vc, ws, outs):
+        for t in range(steps):
+            rkv.kv_cache_scatter(kn[t], vn[t], kc, vc, M, 1, Hk, D, L, pos[t])
+            rkv.attn_decode_batched(qs[t], kc, vc, outs[t], M, H, Hk, D, L, pos[t] + 1, 0.0, ws, n)
+
+    ka, va = kc0.clone(), vc0.clone()
+    wa = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    oa = torch.empty((steps, M, H * D), device="cuda")
+    run(ka, va, wa, oa)
+    torch.cuda.synchronize()
+    kb, vb = kc0.clone(), vc0.clone()
+    wb = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    ob = torch.full((steps, M, H * D), float("nan"), device="cuda")
+    lens_b = pos + 1                      # allocated before capture
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for t in range(steps):
+            rkv.kv_cache_scatter(kn[t], vn[t], kb, vb, M, 1, Hk, D, L, pos[t])
+            rkv.attn_decode_batched(qs[t], kb, vb, ob[t], M, H, Hk, D, L, lens_b[t], 0.0, wb, n)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(ob, oa)
+    assert torch.equal(kb, ka) and torch.equal(vb, va)
