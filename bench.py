@@ -305,7 +305,7 @@ def run_rkv(args, rank, world, torch, dist):
         "clocks": clocks,
     }
     if not args.no_configs:
-        main = {"prefill_tflops": prefill_tflops, "prefill_ms": prefill_ms,
+        main = {"prefill_tflops": prefill_tflops, "prefill_ms": prefill_ms, "fill_ms": fill_ms,
                 "fill_gbs": rooflines["scatter_fill"]["achieved"], "decode_step_gbs": decode_step_gbs,
                 "decode_step_ms": dsc_ms + dec_ms}
         out["configs"], _ = measure_configs(torch, rkv, dev, stream, main, peaks, peak_kind)
@@ -384,7 +384,26 @@ def measure_configs(torch, rkv, dev, stream, main, peaks, peak_kind):
         f"Lmax={L}"] = {"value": tfl, "unit": "TFLOP/s", "ms": ms, "bound": "tensor", "peak": tf32,
                         "frac": tfl / tf32, "launches": 20, "l2": "flushed before each launch",
                         "note": "attn_prefill_chunked; FLOP counted over the keys each token sees"}
-    del q, k, v, kc, vc, q2, o2
+    # the causal GQA prefill with its cache fill fused into the same kernel
+    o3 = torch.empty_like(q)
+    run = lambda: rkv.attn_prefill_fill_cache(q, k, v, o3, P.B, P.S, P.H, P.Hk, P.D, True, kc, vc, L)
+    for _ in range(3):
+        run()
+    ms = time_launches(torch, stream, run, 20, flush)
+    tfl = P.flops / (ms * 1e-3) / 1e12
+    zero = torch.zeros(P.B, dtype=torch.int32, device=dev)
+
+    def run_sep():
+        rkv.attn_prefill(q, k, v, o3, P.B, P.S, P.H, P.Hk, P.D, True)
+        rkv.kv_cache_scatter(k, v, kc, vc, P.B, P.S, P.Hk, P.D, L, zero)
+    run_sep()
+    sep_ms = time_launches(torch, stream, run_sep, 20, flush)
+    out[f"causal GQA prefill B={P.B} S={P.S} H={P.H} Hk={P.Hk} D={P.D} with the cache fill fused"] = {
+        "value": tfl, "unit": "TFLOP/s", "ms": ms, "bound": "tensor", "peak": tf32, "frac": tfl / tf32,
+        "launches": 20, "l2": "flushed before each launch", "separate_ms": sep_ms,
+        "note": "attn_prefill_fill_cache: prefill FLOP over the one kernel's time, which also writes the 67 MB of "
+                "K/V rows into [4,8,4096,128]; separate_ms = attn_prefill then kv_cache_scatter, timed the same way"}
+    del q, k, v, kc, vc, q2, o2, o3
     out[PREFILL.name + " + cache fill"] = {
         "value": main["prefill_tflops"], "unit": "TFLOP/s", "ms": main["prefill_ms"], "bound": "tensor",
         "peak": tf32, "frac": main["prefill_tflops"] / tf32,

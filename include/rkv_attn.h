@@ -100,6 +100,34 @@ rkv_status attn_prefill(const float* q, const float* k, const float* v, float* o
                         int causal, const int* seq_lens, float scale, cudaStream_t stream);
 
 /*
+ * Prefill of fresh sequences fused with their cache fill: attn_prefill (without
+ * seq_lens) plus kv_cache_scatter of all seq_len rows at positions 0..seq_len-1,
+ * in one kernel.
+ *
+ * Cites: trueno-gpu attention.rs, fn batched_multihead_attention_optimized and
+ * trustformers-core attention.rs, fn attention_prefill_gpu_to_gpu (the
+ * attention); realizar cache_from_cache_from_kv_cache.rs, cache filled after a
+ * prefill into [M, num_kv_heads, max_len, head_dim] (the fill).
+ *
+ *   q, k, v, o  as attn_prefill (every row of every sequence valid)
+ *   k_cache,
+ *   v_cache     [batch, n_kv_heads, max_len, head_dim], updated in place:
+ *               cache[b, kh, t, :] = k[b, t, kh*head_dim : (kh+1)*head_dim] for
+ *               t < seq_len (same for v); rows t >= seq_len are untouched.
+ * o is the same as attn_prefill's to the bit, and the cache rows are bit-exact
+ * copies.  Two kernels on `stream`: the prefill, and the fill launched as its
+ * programmatic dependent, which starts at once beside the prefill (in the
+ * registers and shared memory a prefill CTA leaves free on each SM), reads the
+ * K/V rows while the prefill has them in L2, and completes only after the
+ * prefill, so later work on `stream` is ordered after both.  0 <= batch <= 32,
+ * seq_len <= max_len; o and the caches must not alias the inputs or each other.
+ */
+rkv_status attn_prefill_fill_cache(const float* q, const float* k, const float* v, float* o,
+                                   int batch, int seq_len, int n_heads, int n_kv_heads,
+                                   int head_dim, int causal, float scale, float* k_cache,
+                                   float* v_cache, int max_len, cudaStream_t stream);
+
+/*
  * Prefill appended behind rows already in the resident cache (chunked prefill).
  *
  * Cites: trustformers-core attention.rs, fn attention_prefill_gpu_to_gpu (its

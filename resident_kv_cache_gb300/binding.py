@@ -65,6 +65,8 @@ def load():
     lib.rkv_read_device_flags.argtypes = [ctypes.POINTER(ctypes.c_uint), I, P]
     lib.attn_prefill.restype = I
     lib.attn_prefill.argtypes = [P, P, P, P, I, I, I, I, I, I, P, F, P]
+    lib.attn_prefill_fill_cache.restype = I
+    lib.attn_prefill_fill_cache.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, P, I, P]
     lib.attn_prefill_chunked.restype = I
     lib.attn_prefill_chunked.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P, P, F, P]
     lib.attn_decode_workspace_bytes.restype = SZ
@@ -126,6 +128,13 @@ def attn_prefill(q, k, v, o, batch, seq_len, n_heads, n_kv_heads, head_dim, caus
     _check("attn_prefill", load().attn_prefill(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), batch, seq_len, n_heads, n_kv_heads, head_dim,
         int(bool(causal)), _ptr(seq_lens), float(scale), _stream(stream)))
+
+
+def attn_prefill_fill_cache(q, k, v, o, batch, seq_len, n_heads, n_kv_heads, head_dim, causal, k_cache, v_cache,
+                            max_len, scale=0.0, stream=None):
+    _check("attn_prefill_fill_cache", load().attn_prefill_fill_cache(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), batch, seq_len, n_heads, n_kv_heads, head_dim, int(bool(causal)),
+        float(scale), _ptr(k_cache), _ptr(v_cache), max_len, _stream(stream)))
 
 
 def attn_prefill_chunked(q, k_cache, v_cache, o, M, T, n_heads, n_kv_heads, head_dim, max_len, causal,

@@ -56,6 +56,63 @@ kv_scatter_kernel(const float4* __restrict__ k_new, const float4* __restrict__ v
     }
 }
 
+// Cache fill of whole sequences at positions 0..S-1, one persistent CTA per SM (grid-stride over
+// every float4 of K and V).  It is launched as a programmatic dependent of the prefill: its CTAs
+// start beside the prefill's (256 threads and a few registers fit in what a prefill CTA leaves
+// free), read the same inputs the prefill reads and write rows nothing else touches; the final
+// griddepcontrol.wait keeps it from completing before the prefill, so later work in the stream
+// is ordered after both.
+template <int D4>
+__global__ void __launch_bounds__(kScatterThreads)
+kv_fill_kernel(const float4* __restrict__ k, const float4* __restrict__ v, float4* __restrict__ k_cache,
+               float4* __restrict__ v_cache, int S, int Hk, int Lmax, int64_t total) {
+    const int row4 = Hk * D4;                         // float4 elements per token
+#pragma unroll 4
+    for (int64_t idx = (int64_t)blockIdx.x * kScatterThreads + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * kScatterThreads) {
+        const int64_t tok = idx / row4;               // b * S + t
+        const int rem = (int)(idx - tok * row4);
+        const int kh = rem / D4, d4 = rem - kh * D4;
+        const int64_t b = tok / S, t = tok - b * S;
+        const int64_t dst = ((b * Hk + kh) * Lmax + t) * D4 + d4;
+        __stcs(k_cache + dst, __ldg(k + idx));
+        __stcs(v_cache + dst, __ldg(v + idx));
+    }
+    griddep_wait();
+}
+
+rkv_status launch_fill_dependent(const float* k, const float* v, float* k_cache, float* v_cache, int B, int S,
+                                 int Hk, int D, int Lmax, cudaStream_t stream) {
+    const int sms = sm_count();
+    if (sms <= 0) return set_error(RKV_ERR_LAUNCH, "attn_prefill_fill_cache: cannot query the SM count");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)sms);
+    cfg.blockDim = dim3(kScatterThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int64_t total = (int64_t)B * S * Hk * (D / 4);
+    auto k4 = reinterpret_cast<const float4*>(k);
+    auto v4 = reinterpret_cast<const float4*>(v);
+    auto kc = reinterpret_cast<float4*>(k_cache);
+    auto vc = reinterpret_cast<float4*>(v_cache);
+    cudaError_t e;
+    switch (D) {
+        case 16: e = cudaLaunchKernelEx(&cfg, kv_fill_kernel<4>, k4, v4, kc, vc, S, Hk, Lmax, total); break;
+        case 32: e = cudaLaunchKernelEx(&cfg, kv_fill_kernel<8>, k4, v4, kc, vc, S, Hk, Lmax, total); break;
+        case 64: e = cudaLaunchKernelEx(&cfg, kv_fill_kernel<16>, k4, v4, kc, vc, S, Hk, Lmax, total); break;
+        case 128: e = cudaLaunchKernelEx(&cfg, kv_fill_kernel<32>, k4, v4, kc, vc, S, Hk, Lmax, total); break;
+        default: return set_error(RKV_ERR_UNSUPPORTED, "attn_prefill_fill_cache: head_dim %d", D);
+    }
+    if (e != cudaSuccess)
+        return set_error(RKV_ERR_LAUNCH, "attn_prefill_fill_cache: fill launch: %s", cudaGetErrorString(e));
+    return check_launch("attn_prefill_fill_cache");
+}
+
 rkv_status launch_scatter(const float* k_new, const float* v_new, float* k_cache, float* v_cache, int M,
                           int T, int Hk, int D, int Lmax, const int* start_pos, int* overflow,
                           unsigned int* flags, cudaStream_t stream) {

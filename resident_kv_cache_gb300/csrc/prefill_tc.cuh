@@ -179,7 +179,10 @@ __device__ __forceinline__ int pf_item(int k) {
 // then are V rows past the sequence zeroed and padded output rows forced to zero; without
 // it every loaded row is inside the tensors (rows past them are zero-filled by the copy
 // engine and clipped on store) and the kernel carries none of that code.
-template <int D, bool GUARD>
+// FILL: the launch is followed by a programmatic dependent (the cache fill, kv_scatter.cu),
+// which this kernel releases at once so that it runs beside the attention, in the registers and
+// shared memory the prefill leaves free on each SM.
+template <int D, bool GUARD, bool FILL>
 __global__ void __launch_bounds__(kPfThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
@@ -188,6 +191,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                   int n_qtiles, int n_work, const PfKv kv, unsigned int* __restrict__ flags) {
     using C = PfCfg<D>;
     constexpr int BN = C::BN;
+    static_assert(!(FILL && GUARD), "the fused cache fill is built for whole sequences only");
+    if (FILL) griddep_launch_dependents();
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
@@ -782,7 +787,7 @@ static inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-template <int D, bool GUARD>
+template <int D, bool GUARD, bool FILL>
 rkv_status launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
     using C = PfCfg<D>;
     auto encode = tensor_map_encoder();
@@ -822,7 +827,7 @@ rkv_status launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     if (cr != CUDA_SUCCESS) return set_error(RKV_ERR_LAUNCH, "%s: tensor map encode failed (%d)", a.op, (int)cr);
-    auto kern = prefill_tc_kernel<D, GUARD>;
+    auto kern = prefill_tc_kernel<D, GUARD, FILL>;
     static bool attr_done[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -838,9 +843,13 @@ rkv_status launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
     const int sms = sm_count();
     if (sms <= 0) return set_error(RKV_ERR_LAUNCH, "%s: cannot query the SM count", a.op);
     const int grid = (int)(n_work < (int64_t)sms ? n_work : (int64_t)sms);
-    kern<<<grid, kPfThreads, C::SMEM, stream>>>(tm_k, tm_v, tm_q, tm_o, a.o, a.B, a.S, a.H, a.Hk, a.causal ? 1 : 0,
-                                                a.seq_lens, a.scale * kPfLog2e, n_qtiles, (int)n_work, kv, a.flags);
-    return check_launch(a.op);
+    kern<<<grid, kPfThreads, C::SMEM, stream>>>(
+        tm_k, tm_v, tm_q, tm_o, a.o, a.B, a.S, a.H, a.Hk, a.causal ? 1 : 0, a.seq_lens, a.scale * kPfLog2e, n_qtiles,
+        (int)n_work, kv, a.flags);
+    if (check_launch(a.op) != RKV_OK) return RKV_ERR_LAUNCH;
+    if (FILL) return launch_fill_dependent(a.k, a.v, a.k_cache_out, a.v_cache_out, a.B, a.S, a.Hk, D, a.fill_max_len,
+                                           stream);
+    return RKV_OK;
 }
 
 }  // namespace rkv

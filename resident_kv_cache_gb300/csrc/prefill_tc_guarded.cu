@@ -12,10 +12,10 @@ namespace rkv {
 
 rkv_status launch_prefill_guarded(const PrefillArgs& a, cudaStream_t stream) {
     switch (a.D) {
-        case 16: return launch_prefill_tc_t<16, true>(a, stream);
-        case 32: return launch_prefill_tc_t<32, true>(a, stream);
-        case 64: return launch_prefill_tc_t<64, true>(a, stream);
-        case 128: return launch_prefill_tc_t<128, true>(a, stream);
+        case 16: return launch_prefill_tc_t<16, true, false>(a, stream);
+        case 32: return launch_prefill_tc_t<32, true, false>(a, stream);
+        case 64: return launch_prefill_tc_t<64, true, false>(a, stream);
+        case 128: return launch_prefill_tc_t<128, true, false>(a, stream);
     }
     return set_error(RKV_ERR_UNSUPPORTED, "%s: head_dim %d", a.op, a.D);
 }

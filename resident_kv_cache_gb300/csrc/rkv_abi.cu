@@ -162,7 +162,48 @@ rkv_status attn_prefill(const float* q, const float* k, const float* v, float* o
     if ((const void*)o == (const void*)q || (const void*)o == (const void*)k || (const void*)o == (const void*)v)
         return set_error(RKV_ERR_INVALID_ARG, "%s: o must not alias q, k or v", op);
     PrefillArgs a{q, k, v, o, batch, seq_len, n_heads, n_kv_heads, head_dim, causal != 0, seq_lens, sc,
-                  device_flags_ptr(), op, false, 0, nullptr};
+                  device_flags_ptr(), op, false, 0, nullptr, nullptr, nullptr, 0};
+    if (!a.flags) return set_error(RKV_ERR_LAUNCH, "%s: device flag word unavailable", op);
+    return launch_prefill(a, stream);
+}
+
+rkv_status attn_prefill_fill_cache(const float* q, const float* k, const float* v, float* o, int batch,
+                                   int seq_len, int n_heads, int n_kv_heads, int head_dim, int causal, float scale,
+                                   float* k_cache, float* v_cache, int max_len, cudaStream_t stream) {
+    const char* op = "attn_prefill_fill_cache";
+    g_msg[0] = 0;
+    if (batch < 0 || batch > kDecodeMaxSeqs)
+        return set_error(RKV_ERR_INVALID_ARG, "%s: batch must be in [0, %d], got %d", op, kDecodeMaxSeqs, batch);
+    if (seq_len < 0) return set_error(RKV_ERR_INVALID_ARG, "%s: seq_len must be >= 0, got %d", op, seq_len);
+    rkv_status st = check_heads(n_heads, n_kv_heads, head_dim, op);
+    if (st != RKV_OK) return st;
+    if (max_len <= 0) return set_error(RKV_ERR_INVALID_ARG, "%s: max_len must be > 0, got %d", op, max_len);
+    if (seq_len > max_len)
+        return set_error(RKV_ERR_INVALID_ARG, "%s: seq_len (%d) exceeds max_len (%d)", op, seq_len, max_len);
+    float sc;
+    if ((st = resolve_scale(scale, head_dim, sc, op)) != RKV_OK) return st;
+    if (batch == 0 || seq_len == 0) return RKV_OK;
+    if (!q || !k || !v || !o || !k_cache || !v_cache)
+        return set_error(RKV_ERR_INVALID_ARG, "%s: q, k, v, o and the caches must be non-NULL", op);
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16))
+        return set_error(RKV_ERR_INVALID_ARG, "%s: q, k, v, o and the caches must be 16-byte aligned", op);
+    int64_t nq, nkv, nc;
+    if (!elems(nq, {batch, seq_len, n_heads, head_dim}) || !elems(nkv, {batch, seq_len, n_kv_heads, head_dim}) ||
+        !elems(nc, {batch, n_kv_heads, max_len, head_dim}))
+        return set_error(RKV_ERR_INVALID_ARG, "%s: tensor sizes overflow int64", op);
+    if ((int64_t)seq_len * n_kv_heads * head_dim * 4 >= (int64_t(1) << 40) ||
+        (int64_t)max_len * head_dim * 4 >= (int64_t(1) << 40))
+        return set_error(RKV_ERR_UNSUPPORTED, "%s: row stride beyond the kernel's limits", op);
+    const void* outs[3] = {o, k_cache, v_cache};
+    const void* ins[3] = {q, k, v};
+    for (const void* w : outs)
+        for (const void* r : ins)
+            if (w == r) return set_error(RKV_ERR_INVALID_ARG, "%s: o and the caches must not alias q, k or v", op);
+    if ((const void*)o == (const void*)k_cache || (const void*)o == (const void*)v_cache || k_cache == v_cache)
+        return set_error(RKV_ERR_INVALID_ARG, "%s: o, k_cache and v_cache must be distinct", op);
+    PrefillArgs a{q, k, v, o, batch, seq_len, n_heads, n_kv_heads, head_dim, causal != 0, nullptr, sc,
+                  device_flags_ptr(), op, false, 0, nullptr, k_cache, v_cache, max_len};
     if (!a.flags) return set_error(RKV_ERR_LAUNCH, "%s: device flag word unavailable", op);
     return launch_prefill(a, stream);
 }
@@ -196,7 +237,7 @@ rkv_status attn_prefill_chunked(const float* q, const float* k_cache, const floa
         (const void*)o == (const void*)v_cache)
         return set_error(RKV_ERR_INVALID_ARG, "%s: o must not alias q or the caches", op);
     PrefillArgs a{q, k_cache, v_cache, o, M, T, n_heads, n_kv_heads, head_dim, causal != 0, q_lens, sc,
-                  device_flags_ptr(), op, true, max_len, start_pos};
+                  device_flags_ptr(), op, true, max_len, start_pos, nullptr, nullptr, 0};
     if (!a.flags) return set_error(RKV_ERR_LAUNCH, "%s: device flag word unavailable", op);
     return launch_prefill(a, stream);
 }

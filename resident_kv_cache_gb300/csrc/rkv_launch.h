@@ -25,6 +25,9 @@ struct PrefillArgs {
     bool kv_cache;         // K/V read from the cache: query i sits at key position start_pos + i
     int max_len;           // cache capacity (kv_cache)
     const int* start_pos;  // device int32[B] (kv_cache)
+    float* k_cache_out;    // non-NULL: also write K/V rows 0..S-1 into these caches [B, Hk, fill_max_len, D]
+    float* v_cache_out;
+    int fill_max_len;
 };
 
 struct DecodeArgs {
@@ -48,5 +51,11 @@ rkv_status launch_decode(const DecodeArgs& a, cudaStream_t stream);
 rkv_status launch_scatter(const float* k_new, const float* v_new, float* k_cache, float* v_cache, int M,
                           int T, int Hk, int D, int Lmax, const int* start_pos, int* overflow,
                           unsigned int* flags, cudaStream_t stream);
+
+// Cache fill of rows 0..S-1 (K and V [B, S, Hk*D] -> caches [B, Hk, Lmax, D]) launched as a
+// programmatic dependent of the kernel just enqueued on `stream`: it may start while that kernel
+// runs, and completes only after it.
+rkv_status launch_fill_dependent(const float* k, const float* v, float* k_cache, float* v_cache, int B, int S,
+                                 int Hk, int D, int Lmax, cudaStream_t stream);
 
 }  // namespace rkv

@@ -22,7 +22,8 @@ def lib():
 
 def test_library_exports_every_declared_function(lib):
     names = binding.declared_functions()
-    assert set(names) >= {"attn_prefill", "attn_prefill_chunked", "attn_decode_batched", "attn_decode_workspace_bytes",
+    assert set(names) >= {"attn_prefill", "attn_prefill_chunked", "attn_prefill_fill_cache", "attn_decode_batched",
+                          "attn_decode_workspace_bytes",
                           "kv_cache_scatter", "rkv_last_error", "rkv_status_string",
                           "rkv_read_device_flags", "rkv_version"}
     for n in names:
@@ -129,6 +130,23 @@ def test_prefill_chunked_host_validation(lib, args, status):
 def test_prefill_chunked_zero_sized_is_a_noop(lib):
     binding.attn_prefill_chunked(None, None, None, None, 0, 8, 4, 2, 64, 128, 1, None, stream=0)
     binding.attn_prefill_chunked(None, None, None, None, 3, 0, 4, 2, 64, 128, 1, None, stream=0)
+
+
+B_ = 3 * A   # a second fake address for the caches
+@pytest.mark.parametrize("args,status", [
+    ((A, A, A, 2 * A, 33, 8, 4, 2, 64, 1, 0.0, B_, 4 * A, 16), INV),     # batch > 32 (batched cache limit)
+    ((A, A, A, 2 * A, 2, 32, 4, 2, 64, 1, 0.0, B_, 4 * A, 16), INV),     # seq_len > max_len
+    ((A, A, A, 2 * A, 2, 8, 4, 2, 64, 1, 0.0, None, 4 * A, 16), INV),   # NULL cache
+    ((A, A, A, 2 * A, 2, 8, 4, 2, 64, 1, 0.0, A, 4 * A, 16), INV),      # cache aliases q
+    ((A, A, A, 2 * A, 2, 8, 4, 2, 64, 1, 0.0, B_, B_, 16), INV),        # k_cache == v_cache
+    ((A, A, A, 2 * A, 2, 8, 4, 2, 64, 1, 0.0, B_ + 8, 4 * A, 16), INV),  # misaligned cache
+    ((A, A, A, 2 * A, 2, 8, 4, 2, 96, 1, 0.0, B_, 4 * A, 16), UNS),     # head_dim
+    ((A, A, A, 2 * A, 2, 8, 4, 2, 64, 1, -1.0, B_, 4 * A, 16), INV),    # negative scale
+])
+def test_prefill_fill_cache_host_validation(lib, args, status):
+    q, k, v, o, B, S, H, Hk, D, causal, scale, kc, vc, L = args
+    _expect(status, binding.attn_prefill_fill_cache, q, k, v, o, B, S, H, Hk, D, causal, kc, vc, L,
+            scale=scale, stream=0)
 
 
 def test_last_error_is_per_call(lib):
