@@ -14,6 +14,9 @@ Page citations are in the C file's header; the functions here follow it:
               cache layout from realizar cache_from_cache_from_kv_cache.rs,
               fn init_batched_kv_cache_gpu.
   scatter  -- trueno-gpu attention.rs, fn kv_cache_scatter_gpu.
+  rope     -- GPT-NeoX half-split rotary embedding at explicit positions:
+              trustformers-core attention.rs, fn rope_neox_gpu_to_gpu and
+              realizar cache_from_cache_from_kv_cache.rs, fn apply_rope_to_buffer.
   prefill_cached -- a prefill appended behind an existing cache, which
               trustformers-core attention.rs, fn attention_prefill_gpu_to_gpu
               says must run the decode path once per token: query i of the
@@ -80,9 +83,10 @@ def _configure(lib):
     lib.rkv_oracle_decode.argtypes = [P, P, P, P, I, I, I, I, I, P, D]
     lib.rkv_oracle_scatter.argtypes = [P, P, P, P, I, I, I, I, I, P, P]
     lib.rkv_oracle_prefill_cached.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P, P, D]
+    lib.rkv_oracle_rope.argtypes = [P, P, L, I, I, I, P, D]
     for f in ("rkv_oracle_prefill", "rkv_oracle_prefill_rows", "rkv_oracle_prefill_probs",
               "rkv_oracle_decode", "rkv_oracle_scatter", "rkv_oracle_num_threads",
-              "rkv_oracle_prefill_cached"):
+              "rkv_oracle_prefill_cached", "rkv_oracle_rope"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -199,3 +203,17 @@ def prefill_cached(q, k_cache, v_cache, B, T, H, Hk, D, Lmax, causal, start_pos,
     if rc != 0:
         raise ValueError("oracle prefill_cached rejected its arguments (start + length above max_len?)")
     return o
+
+
+def rope(x, n_heads, head_dim, positions, theta=10000.0, rotary_ndims=None):
+    """x [..., n_heads*head_dim] rows at absolute `positions` (one per row), rotated (float64)."""
+    x = _f32(x)
+    rows = x.size // (n_heads * head_dim)
+    assert x.size == rows * n_heads * head_dim
+    pos = _i32(np.broadcast_to(np.asarray(positions, np.int32), (rows,)).copy())
+    out = np.zeros(x.shape, dtype=np.float64)
+    r = head_dim if rotary_ndims is None else int(rotary_ndims)
+    rc = _load().rkv_oracle_rope(_ptr(x), _ptr(out), rows, n_heads, head_dim, r, _ptr(pos), float(theta))
+    if rc != 0:
+        raise ValueError("oracle rope rejected its arguments")
+    return out

@@ -334,3 +334,44 @@ int rkv_oracle_prefill_cached(const float* q, const float* k_c, const float* v_c
     }
     return rc;
 }
+
+/*
+ * Rotary position embedding, GPT-NeoX half-split form, at explicit positions.
+ *
+ * trustformers-core attention.rs, fn rope_neox_gpu_to_gpu (partial RoPE over the
+ * first rotary_ndims of each head, half-split pairs, position offset = absolute
+ * position of the first row) and realizar cache_from_cache_from_kv_cache.rs,
+ * fn apply_rope_to_buffer (NEOX split halves: pair (i, i + half), frequency
+ * 1 / theta^(2i / dim), angle = position * frequency, x1' = x1 cos - x2 sin,
+ * x2' = x1 sin + x2 cos).  With r = rotary_ndims (r = head_dim on the realizar
+ * page), pair i < r/2 joins dims i and i + r/2 and turns by
+ *     angle = pos * theta^(-2i / r);
+ * dims r..head_dim-1 pass through unchanged.
+ *   x, out    : [n_rows, n_heads * head_dim]  (out in double)
+ *   positions : int[n_rows], the absolute position of each row
+ * Returns -1 on invalid shapes (r odd, r > head_dim, theta <= 0).
+ */
+int rkv_oracle_rope(const float* x, double* out, int64_t n_rows, int n_heads, int head_dim,
+                    int rotary_ndims, const int* positions, double theta)
+{
+    if (n_rows < 0 || n_heads <= 0 || head_dim <= 0 || rotary_ndims < 0 || rotary_ndims % 2 != 0 ||
+        rotary_ndims > head_dim || !(theta > 0.0))
+        return -1;
+    const int half = rotary_ndims / 2;
+    for (int64_t row = 0; row < n_rows; ++row) {
+        const double pos = (double)positions[row];
+        for (int h = 0; h < n_heads; ++h) {
+            const float* xh = x + (row * n_heads + h) * (int64_t)head_dim;
+            double* oh = out + (row * n_heads + h) * (int64_t)head_dim;
+            for (int d = 0; d < head_dim; ++d) oh[d] = (double)xh[d];
+            for (int i = 0; i < half; ++i) {
+                const double angle = pos * pow(theta, -2.0 * (double)i / (double)rotary_ndims);
+                const double c = cos(angle), s = sin(angle);
+                const double x1 = (double)xh[i], x2 = (double)xh[i + half];
+                oh[i] = x1 * c - x2 * s;
+                oh[i + half] = x1 * s + x2 * c;
+            }
+        }
+    }
+    return 0;
+}

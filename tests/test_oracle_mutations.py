@@ -34,6 +34,10 @@ MUTATIONS = {
     "chunk_noncausal_sees_capacity": ("n_keys = causal ? p0 + i + 1 : p0 + n;",
                                       "n_keys = causal ? p0 + i + 1 : Lmax;"),
     "chunk_padded_rows_kept": ("if (i < n) n_keys", "if (i < T) n_keys"),
+    "rope_rotation_sign": ("oh[i] = x1 * c - x2 * s;", "oh[i] = x1 * c + x2 * s;"),
+    "rope_adjacent_pairs": ("x2 = (double)xh[i + half];", "x2 = (double)xh[i ^ 1];"),
+    "rope_frequency_over_head_dim": ("(double)i / (double)rotary_ndims", "(double)i / (double)head_dim"),
+    "rope_position_ignored": ("const double pos = (double)positions[row];", "const double pos = 1.0;"),
 }
 
 
@@ -59,6 +63,10 @@ def _pin_checks():
         checks.append(lambda ci=ci: pins.test_prefill_cached_matches_brute_force(om, ci))
     checks.append(lambda: pins.test_prefill_cached_single_token_equals_decode(om))
     checks.append(lambda: pins.test_prefill_cached_chunks_compose_to_full_prefill(om))
+    checks.append(lambda: pins.test_golden_rope(om))
+    checks.append(lambda: pins.test_rope_preserves_pair_norms(om))
+    for r in (8, 16):
+        checks.append(lambda r=r: pins.test_rope_scores_depend_only_on_relative_position(om, r))
     return checks
 
 

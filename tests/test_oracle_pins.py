@@ -443,3 +443,47 @@ def test_prefill_cached_rejects_chunk_past_capacity(oracle_mod):
     kc = inputs.normal((1, 1, 5, 4), 2)
     with pytest.raises(ValueError):
         oracle_mod.prefill_cached(q, kc, kc, 1, 3, 1, 1, 4, 5, True, np.array([3]))
+
+
+# ------------------------------------------------------------ rotary embedding
+def test_golden_rope(oracle_mod):
+    g = _golden("rope_neox_closed_form.json")
+    full = oracle_mod.rope(np.array([g["x_full"]], np.float32), 1, 4, [g["position"]], theta=g["theta"])
+    assert np.max(np.abs(full[0] - np.array(g["expected_full"]))) <= g["tolerance"]
+    part = oracle_mod.rope(np.array([g["x_partial"]], np.float32), 1, 6, [g["position"]], theta=g["theta"],
+                           rotary_ndims=g["rotary_ndims_partial"])
+    assert np.max(np.abs(part[0] - np.array(g["expected_partial"]))) <= g["tolerance"]
+    same = oracle_mod.rope(np.array([g["x_full"]], np.float32), 1, 4, [0], theta=g["theta"])
+    assert np.array_equal(same[0], np.array(g["x_full"], np.float64))
+
+
+def test_rope_preserves_pair_norms(oracle_mod):
+    H, D, r = 3, 16, 12
+    x = inputs.normal((5, H * D), 3001)
+    pos = np.array([0, 1, 17, 4095, 32767])
+    out = oracle_mod.rope(x, H, D, pos, theta=1e6, rotary_ndims=r).reshape(5, H, D)
+    x3 = x.astype(np.float64).reshape(5, H, D)
+    h = r // 2
+    n_in = x3[..., :h] ** 2 + x3[..., h:r] ** 2
+    n_out = out[..., :h] ** 2 + out[..., h:r] ** 2
+    assert np.max(np.abs(n_in - n_out)) < 1e-9
+    assert np.array_equal(out[..., r:], x3[..., r:])       # dims past rotary_ndims untouched
+
+
+@pytest.mark.parametrize("r", [8, 16])
+def test_rope_scores_depend_only_on_relative_position(oracle_mod, r):
+    """q at m and k at n score the same as q at m - n and k at 0: the property RoPE exists for."""
+    D = 16
+    q = inputs.normal((1, D), 3011)
+    k = inputs.normal((1, D), 3012)
+    for m, n in ((5, 3), (100, 100), (4097, 15), (30000, 29000)):
+        a = oracle_mod.rope(q, 1, D, [m], rotary_ndims=r)[0] @ oracle_mod.rope(k, 1, D, [n], rotary_ndims=r)[0]
+        b = oracle_mod.rope(q, 1, D, [m - n], rotary_ndims=r)[0] @ oracle_mod.rope(k, 1, D, [0], rotary_ndims=r)[0]
+        assert abs(a - b) < 1e-9
+
+
+def test_rope_rejects_bad_shapes(oracle_mod):
+    x = inputs.normal((1, 8), 1)
+    for kw in ({"rotary_ndims": 3}, {"rotary_ndims": 10}, {"theta": 0.0}):
+        with pytest.raises(ValueError):
+            oracle_mod.rope(x, 1, 8, [1], **kw)
