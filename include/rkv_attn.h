@@ -242,6 +242,39 @@ rkv_status kv_cache_scatter(const float* k_new, const float* v_new, float* k_cac
                             int max_len, const int* start_pos, int* overflow,
                             cudaStream_t stream);
 
+/*
+ * Rotary position embedding fused with the append: the prologue of a decode
+ * step (T = 1) or of a prefill (T = S) in one pass.
+ *
+ * Cites: trustformers-core attention.rs, fn rope_neox_gpu_to_gpu (GPT-NeoX
+ * half-split partial RoPE over the first rotary_ndims dims of each head, at an
+ * absolute position offset) and realizar cache_from_cache_from_kv_cache.rs,
+ * fn apply_rope_to_buffer (pair (i, i + half), frequency theta^(-2i/dim),
+ * x1' = x1 cos - x2 sin, x2' = x1 sin + x2 cos); the append as kv_cache_scatter.
+ *
+ * For every sequence m and token t, at position p = start_pos[m] + t:
+ *   q      [M, T, n_heads*head_dim]     rotated in place at p (every head)
+ *   k_new  [M, T, n_kv_heads*head_dim]  rotated in place at p
+ *   v_new  [M, T, n_kv_heads*head_dim]  input
+ *   k_cache, v_cache [M, n_kv_heads, max_len, head_dim]: row p receives the
+ *          rotated k and the v row (tokens with p outside [0, max_len) are not
+ *          written and are counted once each in *overflow, if not NULL)
+ * Pair i < rotary_ndims/2 joins dims i and i + rotary_ndims/2 of a head and turns
+ * by p * theta^(-2i/rotary_ndims); dims rotary_ndims.. are unchanged.  The angle
+ * is formed and reduced mod 2*pi in double (frequencies from the host), then
+ * sincosf.  A negative p raises RKV_FLAG_NEGATIVE_INPUT and rotates as p = 0.
+ * 0 <= M <= 32, T <= max_len, rotary_ndims even in (0, head_dim] (a multiple of
+ * 8 is required: RKV_ERR_UNSUPPORTED otherwise), theta > 0; the five tensors
+ * must be distinct.  A decode step is kv_append_rope(T = 1, start_pos = len-1)
+ * then attn_decode_batched with lens; a prefill is kv_append_rope(T = S,
+ * start_pos = 0) then attn_prefill on the rotated q, k (or attn_prefill_chunked
+ * from the cache).
+ */
+rkv_status kv_append_rope(float* q, float* k_new, const float* v_new, float* k_cache,
+                          float* v_cache, int M, int T, int n_heads, int n_kv_heads,
+                          int head_dim, int max_len, const int* start_pos, int rotary_ndims,
+                          float theta, int* overflow, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

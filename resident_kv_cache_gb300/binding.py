@@ -75,6 +75,8 @@ def load():
     lib.attn_decode_batched.argtypes = [P, P, P, P, I, I, I, I, I, P, F, P, SZ, P]
     lib.attn_decode_batched_noalloc.restype = I
     lib.attn_decode_batched_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, P, F, P]
+    lib.kv_append_rope.restype = I
+    lib.kv_append_rope.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, I, F, P, P]
     lib.kv_cache_scatter.restype = I
     lib.kv_cache_scatter.argtypes = [P, P, P, P, I, I, I, I, I, P, P, P]
     _lib = lib
@@ -168,3 +170,12 @@ def kv_cache_scatter(k_new, v_new, k_cache, v_cache, M, T, n_kv_heads, head_dim,
     _check("kv_cache_scatter", load().kv_cache_scatter(
         _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), M, T, n_kv_heads, head_dim, max_len,
         _ptr(start_pos), _ptr(overflow), _stream(stream)))
+
+
+def kv_append_rope(q, k_new, v_new, k_cache, v_cache, M, T, n_heads, n_kv_heads, head_dim, max_len, start_pos,
+                   rotary_ndims=None, theta=10000.0, overflow=None, stream=None):
+    """RoPE (GPT-NeoX half-split) of q and k_new in place at start_pos + t, then K/V into the cache."""
+    _check("kv_append_rope", load().kv_append_rope(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), M, T, n_heads, n_kv_heads, head_dim,
+        max_len, _ptr(start_pos), head_dim if rotary_ndims is None else int(rotary_ndims), float(theta),
+        _ptr(overflow), _stream(stream)))

@@ -284,6 +284,45 @@ rkv_status attn_decode_batched(const float* q, const float* k_cache, const float
     return launch_decode(a, stream);
 }
 
+rkv_status kv_append_rope(float* q, float* k_new, const float* v_new, float* k_cache, float* v_cache, int M, int T,
+                          int n_heads, int n_kv_heads, int head_dim, int max_len, const int* start_pos,
+                          int rotary_ndims, float theta, int* overflow, cudaStream_t stream) {
+    const char* op = "kv_append_rope";
+    g_msg[0] = 0;
+    if (M < 0 || M > kDecodeMaxSeqs)
+        return set_error(RKV_ERR_INVALID_ARG, "%s: M must be in [0, %d], got %d", op, kDecodeMaxSeqs, M);
+    if (T < 0) return set_error(RKV_ERR_INVALID_ARG, "%s: T must be >= 0, got %d", op, T);
+    rkv_status st = check_heads(n_heads, n_kv_heads, head_dim, op);
+    if (st != RKV_OK) return st;
+    if (max_len <= 0) return set_error(RKV_ERR_INVALID_ARG, "%s: max_len must be > 0, got %d", op, max_len);
+    if (T > max_len) return set_error(RKV_ERR_INVALID_ARG, "%s: T (%d) exceeds max_len (%d)", op, T, max_len);
+    if (rotary_ndims <= 0 || rotary_ndims > head_dim || rotary_ndims % 2 != 0)
+        return set_error(RKV_ERR_INVALID_ARG, "%s: rotary_ndims must be even and in (0, head_dim], got %d", op,
+                         rotary_ndims);
+    if (rotary_ndims % 8 != 0)
+        return set_error(RKV_ERR_UNSUPPORTED, "%s: rotary_ndims must be a multiple of 8, got %d", op, rotary_ndims);
+    if (!std::isfinite(theta) || theta <= 0.0f)
+        return set_error(RKV_ERR_INVALID_ARG, "%s: theta must be finite and > 0, got %g", op, (double)theta);
+    if (M == 0 || T == 0) return RKV_OK;
+    if (!q || !k_new || !v_new || !k_cache || !v_cache || !start_pos)
+        return set_error(RKV_ERR_INVALID_ARG, "%s: q, new rows, caches and start_pos must be non-NULL", op);
+    if (!aligned(q, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || !aligned(start_pos, 4) || !aligned(overflow, 4))
+        return set_error(RKV_ERR_INVALID_ARG, "%s: rows and caches must be 16-byte aligned", op);
+    int64_t nq, nn, nc;
+    if (!elems(nq, {M, T, n_heads, head_dim}) || !elems(nn, {M, T, n_kv_heads, head_dim}) ||
+        !elems(nc, {M, n_kv_heads, max_len, head_dim}))
+        return set_error(RKV_ERR_INVALID_ARG, "%s: tensor sizes overflow int64", op);
+    const void* bufs[5] = {q, k_new, v_new, k_cache, v_cache};
+    for (int i = 0; i < 5; ++i)
+        for (int j = i + 1; j < 5; ++j)
+            if (bufs[i] == bufs[j]) return set_error(RKV_ERR_INVALID_ARG, "%s: the five tensors must be distinct", op);
+    unsigned int* flags = device_flags_ptr();
+    if (!flags) return set_error(RKV_ERR_LAUNCH, "%s: device flag word unavailable", op);
+    return launch_rope_append(q, k_new, v_new, k_cache, v_cache, M, T, n_heads, n_kv_heads, head_dim, max_len,
+                              start_pos, rotary_ndims, (double)theta, overflow, flags, stream);
+}
+
 rkv_status kv_cache_scatter(const float* k_new, const float* v_new, float* k_cache, float* v_cache, int M,
                             int T, int n_kv_heads, int head_dim, int max_len, const int* start_pos,
                             int* overflow, cudaStream_t stream) {

@@ -52,6 +52,13 @@ rkv_status launch_scatter(const float* k_new, const float* v_new, float* k_cache
                           int T, int Hk, int D, int Lmax, const int* start_pos, int* overflow,
                           unsigned int* flags, cudaStream_t stream);
 
+// RoPE prologue: q and the new K rows rotated in place at start_pos[m] + t, K (rotated) and V
+// written into the cache (rope_append.cu).  rotary_ndims: multiple of 8, at most head_dim.
+constexpr int kRopeMaxPairs = 64;
+rkv_status launch_rope_append(float* q, float* k_new, const float* v_new, float* k_cache, float* v_cache, int M, int T,
+                              int H, int Hk, int D, int Lmax, const int* start_pos, int rotary_ndims, double theta,
+                              int* overflow, unsigned int* flags, cudaStream_t stream);
+
 // Cache fill of rows 0..S-1 (K and V [B, S, Hk*D] -> caches [B, Hk, Lmax, D]) launched as a
 // programmatic dependent of the kernel just enqueued on `stream`: it may start while that kernel
 // runs, and completes only after it.

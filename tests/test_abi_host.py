@@ -22,7 +22,8 @@ def lib():
 
 def test_library_exports_every_declared_function(lib):
     names = binding.declared_functions()
-    assert set(names) >= {"attn_prefill", "attn_prefill_chunked", "attn_prefill_fill_cache", "attn_decode_batched",
+    assert set(names) >= {"attn_prefill", "attn_prefill_chunked", "attn_prefill_fill_cache", "kv_append_rope",
+                          "attn_decode_batched",
                           "attn_decode_workspace_bytes",
                           "kv_cache_scatter", "rkv_last_error", "rkv_status_string",
                           "rkv_read_device_flags", "rkv_version"}
@@ -147,6 +148,21 @@ def test_prefill_fill_cache_host_validation(lib, args, status):
     q, k, v, o, B, S, H, Hk, D, causal, scale, kc, vc, L = args
     _expect(status, binding.attn_prefill_fill_cache, q, k, v, o, B, S, H, Hk, D, causal, kc, vc, L,
             scale=scale, stream=0)
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"M": 33}, INV), ({"T": 70}, INV), ({"rotary_ndims": 0}, INV), ({"rotary_ndims": 130}, INV),
+    ({"rotary_ndims": 7}, INV), ({"rotary_ndims": 12}, UNS), ({"theta": 0.0}, INV),
+    ({"theta": float("inf")}, INV), ({"head_dim": 96}, UNS), ({"v_cache": B_}, INV), ({"q": A + 4}, INV),
+    ({"start_pos": None}, INV),
+])
+def test_kv_append_rope_host_validation(lib, kw, status):
+    a = dict(q=A, k_new=2 * A, v_new=4 * A, k_cache=B_, v_cache=5 * A, M=2, T=8, n_heads=8, n_kv_heads=2,
+             head_dim=128, max_len=64, start_pos=6 * A, rotary_ndims=128, theta=1e4)
+    a.update(kw)
+    _expect(status, binding.kv_append_rope, a["q"], a["k_new"], a["v_new"], a["k_cache"], a["v_cache"], a["M"],
+            a["T"], a["n_heads"], a["n_kv_heads"], a["head_dim"], a["max_len"], a["start_pos"],
+            rotary_ndims=a["rotary_ndims"], theta=a["theta"], stream=0)
 
 
 def test_last_error_is_per_call(lib):
