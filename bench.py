@@ -411,6 +411,40 @@ def measure_configs(torch, rkv, dev, stream, main, peaks, peak_kind):
     out[DECODE.name] = {"value": main["decode_step_gbs"], "unit": "GB/s", "bound": "hbm", "peak": hbm,
                         "frac": main["decode_step_gbs"] / hbm, "ms": main["decode_step_ms"],
                         "note": "K/V rows attended / (new-row scatter + decode)"}
+    # the batched decode step with the RoPE prologue: kv_append_rope (q and the new K rotated at len-1,
+    # K/V appended) then attn_decode_batched; q, k_new are restored before every step
+    Dd = DECODE
+    xr = inputs.batched_decode_inputs(Dd)
+    kc_r, vc_r = torch.from_numpy(xr["k_cache"]).to(dev), torch.from_numpy(xr["v_cache"]).to(dev)
+    q0, k0 = torch.from_numpy(xr["q"]).to(dev), torch.from_numpy(xr["k_new"]).to(dev)
+    qr, kr = q0.clone(), k0.clone()
+    vr = torch.from_numpy(xr["v_new"]).to(dev)
+    sp_r, ln_r = torch.from_numpy(xr["start_pos"]).to(dev), torch.from_numpy(xr["lens"]).to(dev)
+    od_r = torch.empty((Dd.M, Dd.H * Dd.D), device=dev)
+    nws_r = rkv.attn_decode_workspace_bytes(Dd.M, Dd.H, Dd.Hk, Dd.D, Dd.Lmax)
+    ws_r = torch.zeros(nws_r, dtype=torch.uint8, device=dev)
+
+    def run_rope_step():
+        rkv.kv_append_rope(qr, kr, vr, kc_r, vc_r, Dd.M, 1, Dd.H, Dd.Hk, Dd.D, Dd.Lmax, sp_r, theta=1e6)
+        rkv.attn_decode_batched(qr, kc_r, vc_r, od_r, Dd.M, Dd.H, Dd.Hk, Dd.D, Dd.Lmax, ln_r, 0.0, ws_r, nws_r)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+    for i in range(53):
+        qr.copy_(q0)
+        kr.copy_(k0)
+        if i >= 3:
+            evs[i - 3][0].record(stream)
+        run_rope_step()
+        if i >= 3:
+            evs[i - 3][1].record(stream)
+    torch.cuda.synchronize()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    kv_r, _ = decode_bytes(xr["lens"])
+    gbs = kv_r / (ms * 1e-3) / 1e9
+    out[DECODE.name + " with the RoPE prologue"] = {
+        "value": gbs, "unit": "GB/s", "ms": ms, "bound": "hbm", "peak": hbm, "frac": gbs / hbm, "launches": 100,
+        "note": "kv_append_rope (theta 1e6, full rotary) + attn_decode_batched; K/V rows attended / time of both"}
+    del kc_r, vc_r
+
     d = inputs.LONG_DECODE
     H, Hk, D, L, T = d.H, d.Hk, d.D, d.Lmax, d.extra["steps"]
     kc = torch.from_numpy(inputs.normal((1, Hk, L, D), inputs.SEED_K)).to(dev)

@@ -56,6 +56,8 @@ typedef enum {
 #define RKV_FLAG_WAIT_TIMEOUT    0x1u  /* a bounded on-chip wait gave up; outputs invalid */
 #define RKV_FLAG_LEN_CLAMPED     0x2u  /* a seq_lens entry exceeded its bound and was clamped */
 #define RKV_FLAG_NEGATIVE_INPUT  0x4u  /* a negative length or position was treated as 0 / skipped */
+#define RKV_FLAG_BAD_POINTER     0x8u  /* a per-sequence cache pointer was NULL or not 16-byte aligned: that
+                                          sequence was skipped (no row read or written, zero output) */
 
 /* Library version, (major << 16) | minor. */
 int rkv_version(void);
@@ -219,6 +221,39 @@ rkv_status attn_decode_batched_noalloc(const float* q, const float* k_cache,
                                        const float* v_cache, float* o, int M, int n_heads,
                                        int n_kv_heads, int head_dim, int max_len,
                                        const int* seq_lens, float scale, cudaStream_t stream);
+
+/*
+ * attn_decode_batched over per-sequence caches instead of one batched cache:
+ * the pointer-array layout of realizar cache_from_cache_from_kv_cache.rs, which
+ * keeps device arrays of per-sequence K and V pointers (batched_k_ptrs,
+ * batched_v_ptrs) so each sequence's cache can live anywhere.
+ *
+ *   k_ptrs, v_ptrs  device arrays of M device pointers (8-byte aligned); entry m
+ *                   addresses sequence m's cache [n_kv_heads, max_len, head_dim]
+ *                   and must be 16-byte aligned.  A NULL or misaligned entry is
+ *                   never dereferenced: the sequence is decoded as empty (zero
+ *                   output) and RKV_FLAG_BAD_POINTER is raised.  A pointer to
+ *                   memory that is not a valid cache of that size is the caller's
+ *                   error (it cannot be checked on the device).
+ * Everything else as attn_decode_batched (same kernel, same results).  Rollback
+ * (realizar fn rollback_kv_cache_gpu) needs no call: decoding with a smaller
+ * seq_lens ignores the rows past it.
+ */
+rkv_status attn_decode_batched_ptrs(const float* q, const float* const* k_ptrs,
+                                    const float* const* v_ptrs, float* o, int M, int n_heads,
+                                    int n_kv_heads, int head_dim, int max_len,
+                                    const int* seq_lens, float scale, void* workspace,
+                                    size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * kv_cache_scatter into per-sequence caches (k_ptrs / v_ptrs as for
+ * attn_decode_batched_ptrs; a NULL or misaligned entry skips that sequence's
+ * tokens and raises RKV_FLAG_BAD_POINTER).  Everything else as kv_cache_scatter.
+ */
+rkv_status kv_cache_scatter_ptrs(const float* k_new, const float* v_new, float* const* k_ptrs,
+                                 float* const* v_ptrs, int M, int T, int n_kv_heads, int head_dim,
+                                 int max_len, const int* start_pos, int* overflow,
+                                 cudaStream_t stream);
 
 /*
  * Appends T new K/V rows per sequence into the resident cache.

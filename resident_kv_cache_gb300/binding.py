@@ -19,7 +19,7 @@ LIB_PATH = _build.LIB
 HEADER = os.path.join(_build.INCLUDE, "rkv_attn.h")
 
 RKV_OK, RKV_ERR_INVALID_ARG, RKV_ERR_UNSUPPORTED, RKV_ERR_LAUNCH, RKV_ERR_DEVICE = range(5)
-RKV_FLAG_WAIT_TIMEOUT, RKV_FLAG_LEN_CLAMPED, RKV_FLAG_NEGATIVE_INPUT = 0x1, 0x2, 0x4
+RKV_FLAG_WAIT_TIMEOUT, RKV_FLAG_LEN_CLAMPED, RKV_FLAG_NEGATIVE_INPUT, RKV_FLAG_BAD_POINTER = 0x1, 0x2, 0x4, 0x8
 
 _lib = None
 
@@ -75,6 +75,10 @@ def load():
     lib.attn_decode_batched.argtypes = [P, P, P, P, I, I, I, I, I, P, F, P, SZ, P]
     lib.attn_decode_batched_noalloc.restype = I
     lib.attn_decode_batched_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, P, F, P]
+    lib.attn_decode_batched_ptrs.restype = I
+    lib.attn_decode_batched_ptrs.argtypes = [P, P, P, P, I, I, I, I, I, P, F, P, SZ, P]
+    lib.kv_cache_scatter_ptrs.restype = I
+    lib.kv_cache_scatter_ptrs.argtypes = [P, P, P, P, I, I, I, I, I, P, P, P]
     lib.kv_append_rope.restype = I
     lib.kv_append_rope.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, I, F, P, P]
     lib.kv_cache_scatter.restype = I
@@ -179,3 +183,19 @@ def kv_append_rope(q, k_new, v_new, k_cache, v_cache, M, T, n_heads, n_kv_heads,
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), M, T, n_heads, n_kv_heads, head_dim,
         max_len, _ptr(start_pos), head_dim if rotary_ndims is None else int(rotary_ndims), float(theta),
         _ptr(overflow), _stream(stream)))
+
+
+def attn_decode_batched_ptrs(q, k_ptrs, v_ptrs, o, M, n_heads, n_kv_heads, head_dim, max_len, seq_lens, scale,
+                             workspace, workspace_bytes, stream=None):
+    """attn_decode_batched with per-sequence caches: k_ptrs / v_ptrs are device int64 arrays of M addresses."""
+    _check("attn_decode_batched_ptrs", load().attn_decode_batched_ptrs(
+        _ptr(q), _ptr(k_ptrs), _ptr(v_ptrs), _ptr(o), M, n_heads, n_kv_heads, head_dim, max_len, _ptr(seq_lens),
+        float(scale), _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def kv_cache_scatter_ptrs(k_new, v_new, k_ptrs, v_ptrs, M, T, n_kv_heads, head_dim, max_len, start_pos,
+                          overflow=None, stream=None):
+    """kv_cache_scatter into per-sequence caches (device int64 arrays of M addresses)."""
+    _check("kv_cache_scatter_ptrs", load().kv_cache_scatter_ptrs(
+        _ptr(k_new), _ptr(v_new), _ptr(k_ptrs), _ptr(v_ptrs), M, T, n_kv_heads, head_dim, max_len,
+        _ptr(start_pos), _ptr(overflow), _stream(stream)))

@@ -53,7 +53,8 @@ struct DecCfg {
     static constexpr int REC = ((G * D + 2 * G) + 3) / 4 * 4;      // floats per partial record
     // shared memory layout (bytes): as many K/V stages as fit beside the reduction buffers
     static constexpr int TILE_BYTES = TILE_ROWS * D * 4;
-    static constexpr int SIDE = W * ENTRIES * 4 + W * G * D * 4 + W * 2 * G * 4 + 34 * 8 + 32 * 4 + 2 * 4 * 8 + 16;
+    static constexpr int SIDE = W * ENTRIES * 4 + W * G * D * 4 + W * 2 * G * 4 + 34 * 8 + 32 * 4 + 2 * 4 * 8 + 16 +
+                                2 * 32 * 8;
     static constexpr int NST_FIT = (226 * 1024 - SIDE) / (2 * TILE_BYTES);
     static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;          // pipeline stages
     static_assert(NST >= 2, "decode pipeline needs two stages");
@@ -65,7 +66,8 @@ struct DecCfg {
     static constexpr int OFF_L = OFF_P + 34 * 8;                                  // int L[32]
     static constexpr int OFF_BAR = OFF_L + 32 * 4;                                // full/empty
     static constexpr int OFF_MISC = OFF_BAR + 2 * NST * 8;                        // abort, last
-    static constexpr int SMEM = OFF_MISC + 16;
+    static constexpr int OFF_PTR = OFF_MISC + 16;                                 // per-sequence K, V bases
+    static constexpr int SMEM = OFF_PTR + 2 * 32 * 8;
     static_assert(SMEM <= 227 * 1024, "decode shared memory budget");
     static_assert(NV >= 1 && (LPR & (LPR - 1)) == 0, "lane split");
 };
@@ -121,7 +123,8 @@ __device__ __forceinline__ void locate(int64_t pos, const int64_t* P, const int*
 template <int D, int G>
 __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1)
 decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_cache,
-                      const float* __restrict__ v_cache, float* __restrict__ out, int M, int Hk, int Lmax,
+                      const float* __restrict__ v_cache, const float* const* __restrict__ k_ptrs,
+                      const float* const* __restrict__ v_ptrs, float* __restrict__ out, int M, int Hk, int Lmax,
                       const int* __restrict__ seq_lens, float scale_log2, int* __restrict__ tickets,
                       float* __restrict__ records, unsigned int* __restrict__ flags) {
     using C = DecCfg<D, G>;
@@ -134,6 +137,8 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC);
     volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    const float** kbase = reinterpret_cast<const float**>(smem + C::OFF_PTR);   // [32]
+    const float** vbase = kbase + 32;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -148,6 +153,16 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
             len = __ldg(seq_lens + lane);
             if (len > Lmax) { len = Lmax; atomicOr(flags, RKV_FLAG_LEN_CLAMPED); }
             if (len < 0) { len = 0; atomicOr(flags, RKV_FLAG_NEGATIVE_INPUT); }
+            // the sequence's cache: a slice of the batched cache, or its own allocation (pointer
+            // arrays); a null or misaligned base is never read -- the sequence counts as empty
+            const float* kb = k_ptrs ? k_ptrs[lane] : k_cache + (int64_t)lane * Hk * Lmax * D;
+            const float* vb = v_ptrs ? v_ptrs[lane] : v_cache + (int64_t)lane * Hk * Lmax * D;
+            if (!kb || !vb || ((reinterpret_cast<uintptr_t>(kb) | reinterpret_cast<uintptr_t>(vb)) & 15u)) {
+                len = 0;
+                atomicOr(flags, RKV_FLAG_BAD_POINTER);
+            }
+            kbase[lane] = kb;
+            vbase[lane] = vb;
             L[lane] = len;
         }
         int64_t rows = (int64_t)len * Hk, incl = rows;
@@ -187,7 +202,9 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
                 int64_t seg_start;
                 locate(pos, P, L, Hk, m, kh, seg_start);
                 const int64_t piece_end = min(r1, seg_start + L[m]);
-                const int64_t head_row0 = ((int64_t)m * Hk + kh) * Lmax - seg_start;  // flat -> cache row
+                const int64_t head_row0 = (int64_t)kh * Lmax - seg_start;  // flat -> row of the sequence's cache
+                const float* kb = kbase[m];
+                const float* vb = vbase[m];
                 for (int64_t t0 = pos; t0 < piece_end; t0 += C::TILE_ROWS, ++it) {
                     const int s = it % C::NST;
                     const uint32_t ph = (uint32_t)(it / C::NST) & 1u;
@@ -197,9 +214,9 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
                     const uint32_t full = smem_addr(&bars[s]);
                     mbar_arrive_expect_tx(full, 2 * bytes);
                     const int64_t src = (head_row0 + t0) * D;
-                    bulk_g2s_hint(smem_addr(smem + C::OFF_STAGES + (2 * s) * C::TILE_BYTES), k_cache + src, bytes, full,
+                    bulk_g2s_hint(smem_addr(smem + C::OFF_STAGES + (2 * s) * C::TILE_BYTES), kb + src, bytes, full,
                                   stream_policy);
-                    bulk_g2s_hint(smem_addr(smem + C::OFF_STAGES + (2 * s + 1) * C::TILE_BYTES), v_cache + src, bytes,
+                    bulk_g2s_hint(smem_addr(smem + C::OFF_STAGES + (2 * s + 1) * C::TILE_BYTES), vb + src, bytes,
                                   full, stream_policy);
                     issued[s] = it + 1;
                 }
@@ -474,8 +491,8 @@ static rkv_status launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
     if (n > kDecMaxCtas) n = kDecMaxCtas;
     int* tickets = static_cast<int*>(a.workspace);
     float* records = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + tickets_bytes(a.M, a.Hk));
-    kern<<<n, C::THREADS, C::SMEM, stream>>>(a.q, a.k_cache, a.v_cache, a.o, a.M, a.Hk, a.Lmax, a.seq_lens,
-                                               a.scale * kLog2e, tickets, records, a.flags);
+    kern<<<n, C::THREADS, C::SMEM, stream>>>(a.q, a.k_cache, a.v_cache, a.k_ptrs, a.v_ptrs, a.o, a.M, a.Hk, a.Lmax,
+                                               a.seq_lens, a.scale * kLog2e, tickets, records, a.flags);
     return check_launch("attn_decode_batched");
 }
 

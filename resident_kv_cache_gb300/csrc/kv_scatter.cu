@@ -21,7 +21,8 @@ __global__ void __launch_bounds__(kScatterThreads)
 kv_scatter_kernel(const float4* __restrict__ k_new, const float4* __restrict__ v_new,
                   float4* __restrict__ k_cache, float4* __restrict__ v_cache, int T, int Hk, int Lmax,
                   int tokens_per_block, const int* __restrict__ start_pos, int* __restrict__ overflow,
-                  unsigned int* __restrict__ flags) {
+                  unsigned int* __restrict__ flags, float* const* __restrict__ k_ptrs,
+                  float* const* __restrict__ v_ptrs) {
     const int m = blockIdx.y;
     const int t0 = blockIdx.x * tokens_per_block;
     const int n_tok = min(tokens_per_block, T - t0);
@@ -30,7 +31,14 @@ kv_scatter_kernel(const float4* __restrict__ k_new, const float4* __restrict__ v
     const int row4 = Hk * D4;                         // float4 elements per token
     const int total = n_tok * row4;
     const int64_t src_base = ((int64_t)m * T + t0) * row4;
-    const int64_t seq_base = (int64_t)m * Hk * Lmax;  // first cache row of (m, kh = 0)
+    // the sequence's cache: a slice of the batched cache, or its own allocation (pointer arrays);
+    // a null or misaligned base is never written -- the sequence's tokens are skipped
+    float4* kc = k_ptrs ? reinterpret_cast<float4*>(k_ptrs[m]) : k_cache + (int64_t)m * Hk * Lmax * D4;
+    float4* vc = v_ptrs ? reinterpret_cast<float4*>(v_ptrs[m]) : v_cache + (int64_t)m * Hk * Lmax * D4;
+    if (!kc || !vc || ((reinterpret_cast<uintptr_t>(kc) | reinterpret_cast<uintptr_t>(vc)) & 15u)) {
+        if (threadIdx.x == 0) atomicOr(flags, RKV_FLAG_BAD_POINTER);
+        return;
+    }
 
     if (threadIdx.x < n_tok) {                        // per-token bounds accounting
         const int64_t pos = (int64_t)p0 + t0 + threadIdx.x;
@@ -50,9 +58,9 @@ kv_scatter_kernel(const float4* __restrict__ k_new, const float4* __restrict__ v
         if (pos < 0 || pos >= Lmax) continue;
         const float4 kv = __ldcs(k_new + src_base + idx);
         const float4 vv = __ldcs(v_new + src_base + idx);
-        const int64_t dst = ((seq_base + (int64_t)kh * Lmax) + pos) * D4 + d4;
-        __stcs(k_cache + dst, kv);     // streaming stores: the cache is far larger than L2
-        __stcs(v_cache + dst, vv);
+        const int64_t dst = ((int64_t)kh * Lmax + pos) * D4 + d4;
+        __stcs(kc + dst, kv);          // streaming stores: the cache is far larger than L2
+        __stcs(vc + dst, vv);
     }
 }
 
@@ -115,7 +123,7 @@ rkv_status launch_fill_dependent(const float* k, const float* v, float* k_cache,
 
 rkv_status launch_scatter(const float* k_new, const float* v_new, float* k_cache, float* v_cache, int M,
                           int T, int Hk, int D, int Lmax, const int* start_pos, int* overflow,
-                          unsigned int* flags, cudaStream_t stream) {
+                          unsigned int* flags, cudaStream_t stream, float* const* k_ptrs, float* const* v_ptrs) {
     const int row4 = Hk * (D / 4);
     int tok = kScatterElemsPerBlock / row4;
     if (tok < 1) tok = 1;
@@ -127,10 +135,10 @@ rkv_status launch_scatter(const float* k_new, const float* v_new, float* k_cache
     auto kc = reinterpret_cast<float4*>(k_cache);
     auto vc = reinterpret_cast<float4*>(v_cache);
     switch (D) {
-        case 16: kv_scatter_kernel<4><<<grid, block, 0, stream>>>(k4, v4, kc, vc, T, Hk, Lmax, tok, start_pos, overflow, flags); break;
-        case 32: kv_scatter_kernel<8><<<grid, block, 0, stream>>>(k4, v4, kc, vc, T, Hk, Lmax, tok, start_pos, overflow, flags); break;
-        case 64: kv_scatter_kernel<16><<<grid, block, 0, stream>>>(k4, v4, kc, vc, T, Hk, Lmax, tok, start_pos, overflow, flags); break;
-        case 128: kv_scatter_kernel<32><<<grid, block, 0, stream>>>(k4, v4, kc, vc, T, Hk, Lmax, tok, start_pos, overflow, flags); break;
+        case 16: kv_scatter_kernel<4><<<grid, block, 0, stream>>>(k4, v4, kc, vc, T, Hk, Lmax, tok, start_pos, overflow, flags, k_ptrs, v_ptrs); break;
+        case 32: kv_scatter_kernel<8><<<grid, block, 0, stream>>>(k4, v4, kc, vc, T, Hk, Lmax, tok, start_pos, overflow, flags, k_ptrs, v_ptrs); break;
+        case 64: kv_scatter_kernel<16><<<grid, block, 0, stream>>>(k4, v4, kc, vc, T, Hk, Lmax, tok, start_pos, overflow, flags, k_ptrs, v_ptrs); break;
+        case 128: kv_scatter_kernel<32><<<grid, block, 0, stream>>>(k4, v4, kc, vc, T, Hk, Lmax, tok, start_pos, overflow, flags, k_ptrs, v_ptrs); break;
         default: return set_error(RKV_ERR_UNSUPPORTED, "kv_cache_scatter: head_dim %d", D);
     }
     return check_launch("kv_cache_scatter");

@@ -249,10 +249,12 @@ size_t attn_decode_workspace_bytes(int M, int n_heads, int n_kv_heads, int head_
     return decode_workspace_bytes(M, n_heads, n_kv_heads, head_dim);
 }
 
-rkv_status attn_decode_batched(const float* q, const float* k_cache, const float* v_cache, float* o, int M,
-                               int n_heads, int n_kv_heads, int head_dim, int max_len, const int* seq_lens,
-                               float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-    const char* op = "attn_decode_batched";
+// Batched decode over either the batched cache (k_cache/v_cache) or per-sequence caches
+// (k_ptrs/v_ptrs, device arrays of M pointers).
+static rkv_status decode_entry(const char* op, const float* q, const float* k_cache, const float* v_cache,
+                               const float* const* k_ptrs, const float* const* v_ptrs, float* o, int M, int n_heads,
+                               int n_kv_heads, int head_dim, int max_len, const int* seq_lens, float scale,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     g_msg[0] = 0;
     if (M < 0 || M > kDecodeMaxSeqs)
         return set_error(RKV_ERR_INVALID_ARG, "%s: M must be in [0, %d], got %d", op, kDecodeMaxSeqs, M);
@@ -265,10 +267,11 @@ rkv_status attn_decode_batched(const float* q, const float* k_cache, const float
     if (!decode_group_supported(n_heads / n_kv_heads))
         return set_error(RKV_ERR_UNSUPPORTED, "%s: n_heads/n_kv_heads = %d not supported (1, 2, 4 or 8)", op,
                          n_heads / n_kv_heads);
-    if (!q || !k_cache || !v_cache || !o || !seq_lens || !workspace)
+    const bool ptrs = k_ptrs || v_ptrs;
+    if (!q || !o || !seq_lens || !workspace || (ptrs ? (!k_ptrs || !v_ptrs) : (!k_cache || !v_cache)))
         return set_error(RKV_ERR_INVALID_ARG, "%s: q, caches, o, seq_lens and workspace must be non-NULL", op);
-    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) ||
-        !aligned(workspace, 256) || !aligned(seq_lens, 4))
+    if (!aligned(q, 16) || !aligned(o, 16) || !aligned(workspace, 256) || !aligned(seq_lens, 4) ||
+        (ptrs ? (!aligned(k_ptrs, 8) || !aligned(v_ptrs, 8)) : (!aligned(k_cache, 16) || !aligned(v_cache, 16))))
         return set_error(RKV_ERR_INVALID_ARG,
                          "%s: q, caches and o must be 16-byte aligned, workspace 256-byte aligned", op);
     int64_t nc;
@@ -279,9 +282,24 @@ rkv_status attn_decode_batched(const float* q, const float* k_cache, const float
         return set_error(RKV_ERR_INVALID_ARG, "%s: workspace of %zu bytes is below the %zu required", op,
                          workspace_bytes, need);
     DecodeArgs a{q, k_cache, v_cache, o, M, n_heads, n_kv_heads, head_dim, max_len, seq_lens, sc,
-                 workspace, device_flags_ptr()};
+                 workspace, device_flags_ptr(), k_ptrs, v_ptrs};
     if (!a.flags) return set_error(RKV_ERR_LAUNCH, "%s: device flag word unavailable", op);
     return launch_decode(a, stream);
+}
+
+rkv_status attn_decode_batched(const float* q, const float* k_cache, const float* v_cache, float* o, int M,
+                               int n_heads, int n_kv_heads, int head_dim, int max_len, const int* seq_lens,
+                               float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return decode_entry("attn_decode_batched", q, k_cache, v_cache, nullptr, nullptr, o, M, n_heads, n_kv_heads,
+                        head_dim, max_len, seq_lens, scale, workspace, workspace_bytes, stream);
+}
+
+rkv_status attn_decode_batched_ptrs(const float* q, const float* const* k_ptrs, const float* const* v_ptrs, float* o,
+                                    int M, int n_heads, int n_kv_heads, int head_dim, int max_len,
+                                    const int* seq_lens, float scale, void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream) {
+    return decode_entry("attn_decode_batched_ptrs", q, nullptr, nullptr, k_ptrs, v_ptrs, o, M, n_heads, n_kv_heads,
+                        head_dim, max_len, seq_lens, scale, workspace, workspace_bytes, stream);
 }
 
 rkv_status kv_append_rope(float* q, float* k_new, const float* v_new, float* k_cache, float* v_cache, int M, int T,
@@ -323,10 +341,11 @@ rkv_status kv_append_rope(float* q, float* k_new, const float* v_new, float* k_c
                               start_pos, rotary_ndims, (double)theta, overflow, flags, stream);
 }
 
-rkv_status kv_cache_scatter(const float* k_new, const float* v_new, float* k_cache, float* v_cache, int M,
-                            int T, int n_kv_heads, int head_dim, int max_len, const int* start_pos,
-                            int* overflow, cudaStream_t stream) {
-    const char* op = "kv_cache_scatter";
+// Append into either the batched cache or per-sequence caches (k_ptrs/v_ptrs, device arrays).
+static rkv_status scatter_entry(const char* op, const float* k_new, const float* v_new, float* k_cache,
+                                float* v_cache, float* const* k_ptrs, float* const* v_ptrs, int M, int T,
+                                int n_kv_heads, int head_dim, int max_len, const int* start_pos, int* overflow,
+                                cudaStream_t stream) {
     g_msg[0] = 0;
     if (M < 0 || M > kDecodeMaxSeqs)
         return set_error(RKV_ERR_INVALID_ARG, "%s: M must be in [0, %d], got %d", op, kDecodeMaxSeqs, M);
@@ -338,10 +357,11 @@ rkv_status kv_cache_scatter(const float* k_new, const float* v_new, float* k_cac
                          head_dim);
     if (T > max_len) return set_error(RKV_ERR_INVALID_ARG, "%s: T (%d) exceeds max_len (%d)", op, T, max_len);
     if (M == 0 || T == 0) return RKV_OK;
-    if (!k_new || !v_new || !k_cache || !v_cache || !start_pos)
+    const bool ptrs = k_ptrs || v_ptrs;
+    if (!k_new || !v_new || !start_pos || (ptrs ? (!k_ptrs || !v_ptrs) : (!k_cache || !v_cache)))
         return set_error(RKV_ERR_INVALID_ARG, "%s: new rows, caches and start_pos must be non-NULL", op);
-    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-        !aligned(start_pos, 4) || !aligned(overflow, 4))
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(start_pos, 4) || !aligned(overflow, 4) ||
+        (ptrs ? (!aligned(k_ptrs, 8) || !aligned(v_ptrs, 8)) : (!aligned(k_cache, 16) || !aligned(v_cache, 16))))
         return set_error(RKV_ERR_INVALID_ARG, "%s: rows and caches must be 16-byte aligned", op);
     int64_t nn, nc;
     if (!elems(nn, {M, T, n_kv_heads, head_dim}) || !elems(nc, {M, n_kv_heads, max_len, head_dim}))
@@ -349,7 +369,21 @@ rkv_status kv_cache_scatter(const float* k_new, const float* v_new, float* k_cac
     unsigned int* flags = device_flags_ptr();
     if (!flags) return set_error(RKV_ERR_LAUNCH, "%s: device flag word unavailable", op);
     return launch_scatter(k_new, v_new, k_cache, v_cache, M, T, n_kv_heads, head_dim, max_len, start_pos,
-                          overflow, flags, stream);
+                          overflow, flags, stream, k_ptrs, v_ptrs);
+}
+
+rkv_status kv_cache_scatter(const float* k_new, const float* v_new, float* k_cache, float* v_cache, int M,
+                            int T, int n_kv_heads, int head_dim, int max_len, const int* start_pos,
+                            int* overflow, cudaStream_t stream) {
+    return scatter_entry("kv_cache_scatter", k_new, v_new, k_cache, v_cache, nullptr, nullptr, M, T, n_kv_heads,
+                         head_dim, max_len, start_pos, overflow, stream);
+}
+
+rkv_status kv_cache_scatter_ptrs(const float* k_new, const float* v_new, float* const* k_ptrs, float* const* v_ptrs,
+                                 int M, int T, int n_kv_heads, int head_dim, int max_len, const int* start_pos,
+                                 int* overflow, cudaStream_t stream) {
+    return scatter_entry("kv_cache_scatter_ptrs", k_new, v_new, nullptr, nullptr, k_ptrs, v_ptrs, M, T, n_kv_heads,
+                         head_dim, max_len, start_pos, overflow, stream);
 }
 
 }  // extern "C"

@@ -40,6 +40,8 @@ struct DecodeArgs {
     float scale;
     void* workspace;
     unsigned int* flags;
+    const float* const* k_ptrs = nullptr;   // device float*[M]: per-sequence caches [Hk, Lmax, D]
+    const float* const* v_ptrs = nullptr;   // (then k_cache / v_cache are unused)
 };
 
 rkv_status launch_prefill(const PrefillArgs& a, cudaStream_t stream);
@@ -50,7 +52,8 @@ rkv_status launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 rkv_status launch_scatter(const float* k_new, const float* v_new, float* k_cache, float* v_cache, int M,
                           int T, int Hk, int D, int Lmax, const int* start_pos, int* overflow,
-                          unsigned int* flags, cudaStream_t stream);
+                          unsigned int* flags, cudaStream_t stream, float* const* k_ptrs = nullptr,
+                          float* const* v_ptrs = nullptr);
 
 // RoPE prologue: q and the new K rows rotated in place at start_pos[m] + t, K (rotated) and V
 // written into the cache (rope_append.cu).  rotary_ndims: multiple of 8, at most head_dim.

@@ -23,7 +23,7 @@ def lib():
 def test_library_exports_every_declared_function(lib):
     names = binding.declared_functions()
     assert set(names) >= {"attn_prefill", "attn_prefill_chunked", "attn_prefill_fill_cache", "kv_append_rope",
-                          "attn_decode_batched",
+                          "attn_decode_batched", "attn_decode_batched_ptrs", "kv_cache_scatter_ptrs",
                           "attn_decode_workspace_bytes",
                           "kv_cache_scatter", "rkv_last_error", "rkv_status_string",
                           "rkv_read_device_flags", "rkv_version"}
@@ -163,6 +163,19 @@ def test_kv_append_rope_host_validation(lib, kw, status):
     _expect(status, binding.kv_append_rope, a["q"], a["k_new"], a["v_new"], a["k_cache"], a["v_cache"], a["M"],
             a["T"], a["n_heads"], a["n_kv_heads"], a["head_dim"], a["max_len"], a["start_pos"],
             rotary_ndims=a["rotary_ndims"], theta=a["theta"], stream=0)
+
+
+def test_pointer_array_entries_host_validation(lib):
+    n = binding.attn_decode_workspace_bytes(4, 32, 8, 128, 64)
+    _expect(INV, binding.attn_decode_batched_ptrs, A, None, 2 * A, 3 * A, 4, 32, 8, 128, 64, A, 0.0, A, n, stream=0)
+    _expect(INV, binding.attn_decode_batched_ptrs, A, 2 * A + 4, 3 * A, 4 * A, 4, 32, 8, 128, 64, A, 0.0, A, n,
+            stream=0)                                            # pointer array not 8-byte aligned
+    _expect(INV, binding.attn_decode_batched_ptrs, A, 2 * A, 3 * A, 4 * A, 33, 32, 8, 128, 64, A, 0.0, A, n,
+            stream=0)
+    _expect(INV, binding.kv_cache_scatter_ptrs, A, A, None, 2 * A, 4, 1, 8, 128, 64, A, stream=0)
+    _expect(UNS, binding.kv_cache_scatter_ptrs, A, A, 2 * A, 3 * A, 4, 1, 8, 96, 64, A, stream=0)
+    binding.attn_decode_batched_ptrs(None, None, None, None, 0, 32, 8, 128, 64, None, 0.0, None, 0, stream=0)
+    binding.kv_cache_scatter_ptrs(None, None, None, None, 0, 1, 8, 128, 64, None, stream=0)
 
 
 def test_last_error_is_per_call(lib):
