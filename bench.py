@@ -5,8 +5,8 @@ One step is one pass over every operation of the path:
   1. causal GQA prefill   B=4, S=2048, H=32, Hk=8, D=128   (attn_prefill)
   2. cache fill           its K/V scattered into a [4,8,4096,128] cache (kv_cache_scatter)
   3. batched decode step  M=32, H=32, Hk=8, D=128, cache [32,8,4096,128], lengths U{1..4096}:
-                          the new K/V row scattered at len-1 (kv_cache_scatter), then
-                          attn_decode_batched over len rows.
+                          the new K/V row appended at len-1, then decode over len rows, in
+                          one launch (attn_decode_append).
 The headline value is the decode step's KV-read bandwidth (GB/s of K and V rows
 read); the prefill's TFLOP/s (causal-counted) is reported beside it.  Inputs are
 seeded synthetic N(0,1) f32 and resident in HBM before timing; the per-step
@@ -186,17 +186,14 @@ class Workload:
         P = PREFILL
         self.rkv.kv_cache_scatter(self.k, self.v, self.kc3, self.vc3, P.B, P.S, P.Hk, P.D, FILL_LEN, self.start3)
 
-    def decode_scatter_part(self):
-        Dd = DECODE
-        self.rkv.kv_cache_scatter(self.kn, self.vn, self.kc, self.vc, Dd.M, 1, Dd.Hk, Dd.D, Dd.Lmax, self.sp)
-
     def decode_part(self):
+        """The decode step: each sequence's new row appended at len-1, then decode (one launch)."""
         Dd = DECODE
-        self.rkv.attn_decode_batched(self.qd, self.kc, self.vc, self.od, Dd.M, Dd.H, Dd.Hk, Dd.D, Dd.Lmax,
-                                     self.ln, 0.0, self.ws, self.nws)
+        self.rkv.attn_decode_append(self.qd, self.kn, self.vn, self.kc, self.vc, self.od, Dd.M, Dd.H, Dd.Hk, Dd.D,
+                                    Dd.Lmax, self.ln, 0.0, self.ws, self.nws)
 
 
-LAUNCHES_PER_STEP = 4   # prefill, cache-fill scatter, decode-step scatter, decode
+LAUNCHES_PER_STEP = 3   # prefill, cache-fill scatter, decode step (append + decode)
 
 
 def max_over_ranks(torch, dist, dev, values):
@@ -227,7 +224,7 @@ def run_rkv(args, rank, world, torch, dist):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     W = Workload(torch, rkv, dev)
-    parts = [W.prefill_part, W.fill_part, W.decode_scatter_part, W.decode_part]
+    parts = [W.prefill_part, W.fill_part, W.decode_part]
 
     def step(evs=None):
         for i, fn in enumerate(parts):
@@ -263,10 +260,10 @@ def run_rkv(args, rank, world, torch, dist):
 
     total_ms, *part_ms = max_over_ranks(torch, dist, dev, [total_ms, *part_ms.tolist()])
     ms_step = total_ms / K
-    prefill_ms, fill_ms, dsc_ms, dec_ms = part_ms
+    prefill_ms, fill_ms, dec_ms = part_ms
 
     kv_bytes, dec_all_bytes = decode_bytes(W.lens)
-    decode_step_gbs, value = decode_step_value(kv_bytes, dsc_ms, dec_ms, world)
+    decode_step_gbs, value = decode_step_value(kv_bytes, 0.0, dec_ms, world)
     prefill_tflops = PREFILL.flops / (prefill_ms * 1e-3) / 1e12
     peaks, peak_kind = load_peaks()
     hbm = peaks["hbm_gbs"]
@@ -297,8 +294,7 @@ def run_rkv(args, rank, world, torch, dist):
         "values": {"decode_step_kv_read_gbs": decode_step_gbs, "decode_kernel_gbs":
                    rooflines["decode"]["achieved"], "prefill_tflops": prefill_tflops,
                    "cache_fill_gbs": rooflines["scatter_fill"]["achieved"]},
-        "parts_ms": {"prefill": prefill_ms, "cache_fill_scatter": fill_ms, "decode_scatter": dsc_ms,
-                     "decode": dec_ms},
+        "parts_ms": {"prefill": prefill_ms, "cache_fill_scatter": fill_ms, "decode_step": dec_ms},
         "roofline": dict(rooflines[dominant], kernel=dominant),
         "rooflines": rooflines,
         "gpu_launches": LAUNCHES_PER_STEP * K,
@@ -307,7 +303,7 @@ def run_rkv(args, rank, world, torch, dist):
     if not args.no_configs:
         main = {"prefill_tflops": prefill_tflops, "prefill_ms": prefill_ms, "fill_ms": fill_ms,
                 "fill_gbs": rooflines["scatter_fill"]["achieved"], "decode_step_gbs": decode_step_gbs,
-                "decode_step_ms": dsc_ms + dec_ms}
+                "decode_step_ms": dec_ms}
         out["configs"], _ = measure_configs(torch, rkv, dev, stream, main, peaks, peak_kind)
         if rkv.rkv_read_device_flags() & rkv.RKV_FLAG_WAIT_TIMEOUT:
             raise RuntimeError("device reported a wait timeout during the per-workload runs")
@@ -410,7 +406,7 @@ def measure_configs(torch, rkv, dev, stream, main, peaks, peak_kind):
         "cache_fill_gbs": main["fill_gbs"], "cache_fill_frac": main["fill_gbs"] / hbm}
     out[DECODE.name] = {"value": main["decode_step_gbs"], "unit": "GB/s", "bound": "hbm", "peak": hbm,
                         "frac": main["decode_step_gbs"] / hbm, "ms": main["decode_step_ms"],
-                        "note": "K/V rows attended / (new-row scatter + decode)"}
+                        "note": "K/V rows attended / time of attn_decode_append (new rows appended, then decode)"}
     # the batched decode step with the RoPE prologue: kv_append_rope (q and the new K rotated at len-1,
     # K/V appended) then attn_decode_batched; q, k_new are restored before every step
     Dd = DECODE
@@ -423,6 +419,17 @@ def measure_configs(torch, rkv, dev, stream, main, peaks, peak_kind):
     od_r = torch.empty((Dd.M, Dd.H * Dd.D), device=dev)
     nws_r = rkv.attn_decode_workspace_bytes(Dd.M, Dd.H, Dd.Hk, Dd.D, Dd.Lmax)
     ws_r = torch.zeros(nws_r, dtype=torch.uint8, device=dev)
+
+    def run_two_launch_step():
+        rkv.kv_cache_scatter(k0, vr, kc_r, vc_r, Dd.M, 1, Dd.Hk, Dd.D, Dd.Lmax, sp_r)
+        rkv.attn_decode_batched(q0, kc_r, vc_r, od_r, Dd.M, Dd.H, Dd.Hk, Dd.D, Dd.Lmax, ln_r, 0.0, ws_r, nws_r)
+    run_two_launch_step()
+    ms2 = time_launches(torch, stream, run_two_launch_step, 50)
+    kv_r, _ = decode_bytes(xr["lens"])
+    out[DECODE.name + " as two launches"] = {
+        "value": kv_r / (ms2 * 1e-3) / 1e9, "unit": "GB/s", "ms": ms2, "bound": "hbm", "peak": hbm,
+        "frac": kv_r / (ms2 * 1e-3) / 1e9 / hbm, "launches": 100,
+        "note": "kv_cache_scatter then attn_decode_batched, alone (not after a prefill), back to back"}
 
     def run_rope_step():
         rkv.kv_append_rope(qr, kr, vr, kc_r, vc_r, Dd.M, 1, Dd.H, Dd.Hk, Dd.D, Dd.Lmax, sp_r, theta=1e6)
@@ -438,7 +445,6 @@ def measure_configs(torch, rkv, dev, stream, main, peaks, peak_kind):
             evs[i - 3][1].record(stream)
     torch.cuda.synchronize()
     ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
-    kv_r, _ = decode_bytes(xr["lens"])
     gbs = kv_r / (ms * 1e-3) / 1e9
     out[DECODE.name + " with the RoPE prologue"] = {
         "value": gbs, "unit": "GB/s", "ms": ms, "bound": "hbm", "peak": hbm, "frac": gbs / hbm, "launches": 100,
@@ -461,8 +467,7 @@ def measure_configs(torch, rkv, dev, stream, main, peaks, peak_kind):
 
     def run_long():
         for t in range(T):
-            rkv.kv_cache_scatter(kn[t], vn[t], kc, vc, 1, 1, Hk, D, L, pos[t:t + 1])
-            rkv.attn_decode_batched(qs[t], kc, vc, od, 1, H, Hk, D, L, lens[t:t + 1], 0.0, ws, nws)
+            rkv.attn_decode_append(qs[t], kn[t], vn[t], kc, vc, od, 1, H, Hk, D, L, lens[t:t + 1], 0.0, ws, nws)
 
     run_long()
     ms_eager = time_launches(torch, stream, run_long, 3)
@@ -475,13 +480,13 @@ def measure_configs(torch, rkv, dev, stream, main, peaks, peak_kind):
     kv = sum(2.0 * Hk * x["len"] * D * 4 for x in steps)
     gbs = kv / (ms * 1e-3) / 1e9
     out[d.name] = {"value": gbs, "unit": "GB/s", "ms": ms, "bound": "hbm", "peak": hbm, "frac": gbs / hbm,
-                   "launches": 2 * T, "eager_gbs": kv / (ms_eager * 1e-3) / 1e9, "eager_ms": ms_eager,
-                   "note": f"256 append+decode steps (scatter + decode each), {kv / 1e9:.2f} GB of K/V rows "
+                   "launches": T, "eager_gbs": kv / (ms_eager * 1e-3) / 1e9, "eager_ms": ms_eager,
+                   "note": f"256 append+decode steps (attn_decode_append each), {kv / 1e9:.2f} GB of K/V rows "
                    "read, replayed from one CUDA graph; eager_* = the same launches issued one by one"}
     for v in out.values():
         v["peak_note"] = f"{peak_kind} " + ("copy bandwidth" if v["bound"] == "hbm" else
                                             "bf16 burst x nominal TF32/BF16 ratio 1.1/2.25")
-    return out, 2 * T
+    return out, T
 
 
 def run_e2e(W, torch, rkv, stream, K):
@@ -506,7 +511,6 @@ def run_e2e(W, torch, rkv, stream, K):
         evs[1].record(stream)
         W.qd.copy_(hqd, non_blocking=True); W.kn.copy_(hkn, non_blocking=True); W.vn.copy_(hvn, non_blocking=True)
         W.sp.copy_(hsp, non_blocking=True); W.ln.copy_(hln, non_blocking=True)
-        W.decode_scatter_part()
         W.decode_part()
         hod.copy_(W.od, non_blocking=True)
         evs[2].record(stream)

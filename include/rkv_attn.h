@@ -223,6 +223,31 @@ rkv_status attn_decode_batched_noalloc(const float* q, const float* k_cache,
                                        const int* seq_lens, float scale, cudaStream_t stream);
 
 /*
+ * One decode step in one launch: append each sequence's new K/V row at
+ * position seq_lens[m] - 1, then decode over seq_lens[m] rows -- the same
+ * results, cache and output, as kv_cache_scatter(k_new, v_new, ..., T = 1,
+ * start_pos = seq_lens - 1) followed by attn_decode_batched.
+ *
+ * Cites: trueno-gpu attention.rs, fn kv_cache_scatter_gpu then
+ * fn incremental_attention_gpu (append the token, then attend to rows
+ * 0..seq_len-1); realizar batched cache layout.
+ *
+ *   k_new, v_new  [M, n_kv_heads*head_dim]  the step's new rows
+ *   k_cache, v_cache                        updated in place at row seq_lens[m]-1
+ *                                           (not written when that row is
+ *                                           outside [0, max_len))
+ * Every other argument as attn_decode_batched.  The row of a (sequence, kv
+ * head) is written by the one CTA that also reads it, before its bulk copies
+ * start, so no separate launch or grid-wide ordering is needed.  Outputs must
+ * not alias the inputs.
+ */
+rkv_status attn_decode_append(const float* q, const float* k_new, const float* v_new,
+                              float* k_cache, float* v_cache, float* o, int M, int n_heads,
+                              int n_kv_heads, int head_dim, int max_len, const int* seq_lens,
+                              float scale, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
+
+/*
  * attn_decode_batched over per-sequence caches instead of one batched cache:
  * the pointer-array layout of realizar cache_from_cache_from_kv_cache.rs, which
  * keeps device arrays of per-sequence K and V pointers (batched_k_ptrs,

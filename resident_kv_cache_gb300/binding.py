@@ -75,6 +75,8 @@ def load():
     lib.attn_decode_batched.argtypes = [P, P, P, P, I, I, I, I, I, P, F, P, SZ, P]
     lib.attn_decode_batched_noalloc.restype = I
     lib.attn_decode_batched_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, P, F, P]
+    lib.attn_decode_append.restype = I
+    lib.attn_decode_append.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, F, P, SZ, P]
     lib.attn_decode_batched_ptrs.restype = I
     lib.attn_decode_batched_ptrs.argtypes = [P, P, P, P, I, I, I, I, I, P, F, P, SZ, P]
     lib.kv_cache_scatter_ptrs.restype = I
@@ -199,3 +201,11 @@ def kv_cache_scatter_ptrs(k_new, v_new, k_ptrs, v_ptrs, M, T, n_kv_heads, head_d
     _check("kv_cache_scatter_ptrs", load().kv_cache_scatter_ptrs(
         _ptr(k_new), _ptr(v_new), _ptr(k_ptrs), _ptr(v_ptrs), M, T, n_kv_heads, head_dim, max_len,
         _ptr(start_pos), _ptr(overflow), _stream(stream)))
+
+
+def attn_decode_append(q, k_new, v_new, k_cache, v_cache, o, M, n_heads, n_kv_heads, head_dim, max_len, seq_lens,
+                       scale, workspace, workspace_bytes, stream=None):
+    """One decode step: append the new rows at seq_lens-1, then decode (one launch)."""
+    _check("attn_decode_append", load().attn_decode_append(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(o), M, n_heads, n_kv_heads, head_dim,
+        max_len, _ptr(seq_lens), float(scale), _ptr(workspace), int(workspace_bytes), _stream(stream)))

@@ -126,7 +126,8 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
                       const float* __restrict__ v_cache, const float* const* __restrict__ k_ptrs,
                       const float* const* __restrict__ v_ptrs, float* __restrict__ out, int M, int Hk, int Lmax,
                       const int* __restrict__ seq_lens, float scale_log2, int* __restrict__ tickets,
-                      float* __restrict__ records, unsigned int* __restrict__ flags) {
+                      float* __restrict__ records, unsigned int* __restrict__ flags,
+                      const float* __restrict__ k_new, const float* __restrict__ v_new) {
     using C = DecCfg<D, G>;
     extern __shared__ __align__(1024) unsigned char smem[];
     float* sc_all = reinterpret_cast<float*>(smem + C::OFF_SC);
@@ -185,6 +186,30 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
 
     const int64_t R = P[M];
     const int64_t r0 = share_begin(c, R, n), r1 = share_begin(c + 1, R, n);
+
+    if (k_new) {
+        // Fused append: the new K/V row of each (sequence, kv head) goes to cache row len-1 first.
+        // That row is read by exactly one CTA -- the one whose share holds it -- so that CTA writes
+        // it here, and a proxy fence orders the stores before its own bulk copies read the row.
+        // (A row past max_len is not written, as kv_cache_scatter skips it.)
+        for (int sg = warp; sg < M * Hk && warp < C::W; sg += C::W) {
+            const int m = sg / Hk, kh = sg - m * Hk;
+            const int p = __ldg(seq_lens + m) - 1;        // append position, from the unclamped length
+            if (p < 0 || p >= Lmax || L[m] == 0) continue;
+            const int64_t flat = P[m] + (int64_t)kh * L[m] + p;
+            if (flat < r0 || flat >= r1) continue;
+            const float4* kn = reinterpret_cast<const float4*>(k_new + ((int64_t)m * Hk + kh) * D);
+            const float4* vn = reinterpret_cast<const float4*>(v_new + ((int64_t)m * Hk + kh) * D);
+            float4* kd = reinterpret_cast<float4*>(const_cast<float*>(kbase[m]) + ((int64_t)kh * Lmax + p) * D);
+            float4* vd = reinterpret_cast<float4*>(const_cast<float*>(vbase[m]) + ((int64_t)kh * Lmax + p) * D);
+            for (int i = lane; i < D / 4; i += 32) {
+                kd[i] = __ldg(kn + i);
+                vd[i] = __ldg(vn + i);
+            }
+        }
+        fence_proxy_async_global();
+        __syncthreads();
+    }
 
     if (warp == C::W) {
         // ================================================================ producer
@@ -492,7 +517,8 @@ static rkv_status launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
     int* tickets = static_cast<int*>(a.workspace);
     float* records = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + tickets_bytes(a.M, a.Hk));
     kern<<<n, C::THREADS, C::SMEM, stream>>>(a.q, a.k_cache, a.v_cache, a.k_ptrs, a.v_ptrs, a.o, a.M, a.Hk, a.Lmax,
-                                               a.seq_lens, a.scale * kLog2e, tickets, records, a.flags);
+                                               a.seq_lens, a.scale * kLog2e, tickets, records, a.flags, a.k_new,
+                                               a.v_new);
     return check_launch("attn_decode_batched");
 }
 

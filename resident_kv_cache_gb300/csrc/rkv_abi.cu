@@ -254,7 +254,8 @@ size_t attn_decode_workspace_bytes(int M, int n_heads, int n_kv_heads, int head_
 static rkv_status decode_entry(const char* op, const float* q, const float* k_cache, const float* v_cache,
                                const float* const* k_ptrs, const float* const* v_ptrs, float* o, int M, int n_heads,
                                int n_kv_heads, int head_dim, int max_len, const int* seq_lens, float scale,
-                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                               const float* k_new = nullptr, const float* v_new = nullptr) {
     g_msg[0] = 0;
     if (M < 0 || M > kDecodeMaxSeqs)
         return set_error(RKV_ERR_INVALID_ARG, "%s: M must be in [0, %d], got %d", op, kDecodeMaxSeqs, M);
@@ -282,7 +283,7 @@ static rkv_status decode_entry(const char* op, const float* q, const float* k_ca
         return set_error(RKV_ERR_INVALID_ARG, "%s: workspace of %zu bytes is below the %zu required", op,
                          workspace_bytes, need);
     DecodeArgs a{q, k_cache, v_cache, o, M, n_heads, n_kv_heads, head_dim, max_len, seq_lens, sc,
-                 workspace, device_flags_ptr(), k_ptrs, v_ptrs};
+                 workspace, device_flags_ptr(), k_ptrs, v_ptrs, k_new, v_new};
     if (!a.flags) return set_error(RKV_ERR_LAUNCH, "%s: device flag word unavailable", op);
     return launch_decode(a, stream);
 }
@@ -292,6 +293,28 @@ rkv_status attn_decode_batched(const float* q, const float* k_cache, const float
                                float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     return decode_entry("attn_decode_batched", q, k_cache, v_cache, nullptr, nullptr, o, M, n_heads, n_kv_heads,
                         head_dim, max_len, seq_lens, scale, workspace, workspace_bytes, stream);
+}
+
+rkv_status attn_decode_append(const float* q, const float* k_new, const float* v_new, float* k_cache, float* v_cache,
+                              float* o, int M, int n_heads, int n_kv_heads, int head_dim, int max_len,
+                              const int* seq_lens, float scale, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream) {
+    const char* op = "attn_decode_append";
+    if (M > 0 && M <= kDecodeMaxSeqs) {
+        g_msg[0] = 0;
+        if (!k_new || !v_new)
+            return set_error(RKV_ERR_INVALID_ARG, "%s: k_new and v_new must be non-NULL", op);
+        if (!aligned(k_new, 16) || !aligned(v_new, 16))
+            return set_error(RKV_ERR_INVALID_ARG, "%s: k_new and v_new must be 16-byte aligned", op);
+        const void* ins[3] = {q, k_new, v_new};
+        for (const void* w : {(const void*)k_cache, (const void*)v_cache, (const void*)o})
+            for (const void* r : ins)
+                if (w && w == r) return set_error(RKV_ERR_INVALID_ARG, "%s: outputs must not alias the inputs", op);
+        if (k_cache && k_cache == v_cache)
+            return set_error(RKV_ERR_INVALID_ARG, "%s: k_cache and v_cache must be distinct", op);
+    }
+    return decode_entry(op, q, k_cache, v_cache, nullptr, nullptr, o, M, n_heads, n_kv_heads, head_dim, max_len,
+                        seq_lens, scale, workspace, workspace_bytes, stream, k_new, v_new);
 }
 
 rkv_status attn_decode_batched_ptrs(const float* q, const float* const* k_ptrs, const float* const* v_ptrs, float* o,

@@ -42,6 +42,8 @@ struct DecodeArgs {
     unsigned int* flags;
     const float* const* k_ptrs = nullptr;   // device float*[M]: per-sequence caches [Hk, Lmax, D]
     const float* const* v_ptrs = nullptr;   // (then k_cache / v_cache are unused)
+    const float* k_new = nullptr;           // non-NULL: append [M, Hk*D] rows at len-1 first (fused)
+    const float* v_new = nullptr;
 };
 
 rkv_status launch_prefill(const PrefillArgs& a, cudaStream_t stream);

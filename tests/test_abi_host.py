@@ -24,6 +24,7 @@ def test_library_exports_every_declared_function(lib):
     names = binding.declared_functions()
     assert set(names) >= {"attn_prefill", "attn_prefill_chunked", "attn_prefill_fill_cache", "kv_append_rope",
                           "attn_decode_batched", "attn_decode_batched_ptrs", "kv_cache_scatter_ptrs",
+                          "attn_decode_append",
                           "attn_decode_workspace_bytes",
                           "kv_cache_scatter", "rkv_last_error", "rkv_status_string",
                           "rkv_read_device_flags", "rkv_version"}
@@ -176,6 +177,19 @@ def test_pointer_array_entries_host_validation(lib):
     _expect(UNS, binding.kv_cache_scatter_ptrs, A, A, 2 * A, 3 * A, 4, 1, 8, 96, 64, A, stream=0)
     binding.attn_decode_batched_ptrs(None, None, None, None, 0, 32, 8, 128, 64, None, 0.0, None, 0, stream=0)
     binding.kv_cache_scatter_ptrs(None, None, None, None, 0, 1, 8, 128, 64, None, stream=0)
+
+
+def test_decode_append_host_validation(lib):
+    n = binding.attn_decode_workspace_bytes(4, 32, 8, 128, 64)
+    _expect(INV, binding.attn_decode_append, A, None, 2 * A, 3 * A, 4 * A, 5 * A, 4, 32, 8, 128, 64, A, 0.0, A, n,
+            stream=0)                                              # k_new NULL
+    _expect(INV, binding.attn_decode_append, A, 2 * A, 2 * A + 8, 3 * A, 4 * A, 5 * A, 4, 32, 8, 128, 64, A, 0.0, A,
+            n, stream=0)                                           # v_new misaligned
+    _expect(INV, binding.attn_decode_append, A, 2 * A, 6 * A, 2 * A, 4 * A, 5 * A, 4, 32, 8, 128, 64, A, 0.0, A, n,
+            stream=0)                                              # k_cache aliases k_new
+    _expect(INV, binding.attn_decode_append, A, 2 * A, 6 * A, 3 * A, 3 * A, 5 * A, 4, 32, 8, 128, 64, A, 0.0, A, n,
+            stream=0)                                              # k_cache == v_cache
+    binding.attn_decode_append(None, None, None, None, None, None, 0, 32, 8, 128, 64, None, 0.0, None, 0, stream=0)
 
 
 def test_last_error_is_per_call(lib):
