@@ -444,34 +444,56 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
             named_barrier(1, C::CT);
             if (threadIdx.x == 0) {
                 // pieces = CTAs in [c_first, c_last] that own rows (a share is empty only when R < n)
-                int pieces = 0;
-                for (int cc = c_first; cc <= c_last; ++cc)
-                    pieces += share_begin(cc, R, n) < share_begin(cc + 1, R, n);
+                int pieces = c_last - c_first + 1;
+                if (R < n) {
+                    pieces = 0;
+                    for (int cc = c_first; cc <= c_last; ++cc)
+                        pieces += share_begin(cc, R, n) < share_begin(cc + 1, R, n);
+                }
                 int last = 0;
                 if (ok) last = (atomicAdd(tickets + sg, 1) == pieces - 1);
                 *last_flag = last;
             }
             named_barrier(1, C::CT);
             if (*last_flag) {
+                // Log-sum-exp merge of the segment's records, one warp per query head: the lanes
+                // find the largest running max together, then walk the records once -- m and l
+                // are the same address for every lane (one broadcast load), each lane takes a
+                // float4 of o -- four records at a time so their loads overlap.
                 __threadfence();
-                for (int i = threadIdx.x; i < G * D; i += C::CT) {
-                    const int h = i / D;
+                const bool all_owned = R >= n;          // then every CTA in [c_first, c_last] has a record
+                for (int h = warp; h < G; h += C::W) {
                     float mx = -INFINITY;
-                    for (int cc = c_first; cc <= c_last; ++cc)
-                        if (share_begin(cc, R, n) < share_begin(cc + 1, R, n))
+                    for (int cc = c_first + lane; cc <= c_last; cc += 32)
+                        if (all_owned || share_begin(cc, R, n) < share_begin(cc + 1, R, n))
                             mx = fmaxf(mx, __ldcg(records + (int64_t)(sg + cc) * C::REC + G * D + h));
-                    float l = 0.0f, o = 0.0f;
+#pragma unroll
+                    for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    float l = 0.0f;
+                    float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const bool has_col = lane < D / 4;
                     if (mx != -INFINITY) {
+#pragma unroll 4
                         for (int cc = c_first; cc <= c_last; ++cc) {
-                            if (share_begin(cc, R, n) >= share_begin(cc + 1, R, n)) continue;
+                            if (!all_owned && !(share_begin(cc, R, n) < share_begin(cc + 1, R, n))) continue;
                             const float* rec = records + (int64_t)(sg + cc) * C::REC;
                             const float mc = __ldcg(rec + G * D + h);
+                            const float lc = __ldcg(rec + G * D + G + h);
+                            const float4 oc = has_col ? __ldcg(reinterpret_cast<const float4*>(rec + h * D) + lane)
+                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
                             const float f = (mc == -INFINITY) ? 0.0f : fast_exp2(mc - mx);
-                            l += __ldcg(rec + G * D + G + h) * f;
-                            o += __ldcg(rec + i) * f;
+                            l += lc * f;
+                            o4.x += oc.x * f;
+                            o4.y += oc.y * f;
+                            o4.z += oc.z * f;
+                            o4.w += oc.w * f;
                         }
                     }
-                    o_seg[i] = l > 0.0f ? o / l : 0.0f;
+                    if (has_col) {
+                        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+                        reinterpret_cast<float4*>(o_seg + h * D)[lane] =
+                            make_float4(o4.x * inv, o4.y * inv, o4.z * inv, o4.w * inv);
+                    }
                 }
                 if (threadIdx.x == 0) tickets[sg] = 0;
             }
