@@ -35,7 +35,7 @@
 //                TMA box, conflict-free).
 //   warps 6-9    V transposer: tcgen05 kind::tf32 reads B only K-major, so each
 //                V tile is transposed in shared memory (4x4 blocks through
-//                registers, conflict-free 16-byte stores, 128-byte swizzle).
+//                registers, conflict-free 16-byte loads and stores, 128-byte swizzle).
 // Q, K and V stay f32; the tensor core reads them as TF32 by truncation.
 // Every mbarrier wait is time-bounded (see rkv_internal.cuh); a CTA that gives
 // up unwinds: it drains its own copies in flight, lets issued MMAs finish and
@@ -502,17 +502,36 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         // V tiles arrive by TMA in the same swizzled layout as K (rows = keys).  The
         // transposer rewrites each slot in place as V^T: work item = (key quad aa,
         // d quad dq), a 4x4 block read with four 16-byte loads and written as four
-        // 16-byte rows of V^T.  Lane numbering puts 4 consecutive key quads x 2 d
-        // quads (D = 16: 8 key quads x 1) in each quarter-warp, so its eight V^T
-        // stores hit eight distinct 128-byte-swizzle chunks: no conflicts.
+        // 16-byte rows of V^T.  A 16-byte access is served a quarter-warp at a time, so
+        // the eight lanes of a quarter-warp must hit eight distinct 16-byte chunks of the
+        // 128-byte swizzle, on the loads (chunk (dq ^ key) & 7) and on the stores (chunk
+        // (aa ^ d) & 7).  For D >= 32 a quarter-warp takes a diagonal: lane q gets key quad
+        // 8*ah + q and d quad 8*dh + (q ^ s), with (s, ah, dh) fixed per quarter-warp and
+        // iteration; then both chunk sets are permutations of 0..7.  At D = 16 (64-byte
+        // swizzle) a quarter-warp takes 8 consecutive key quads of one d quad.
         const int wv = warp - kPfVWarp0;                      // 0..3
-        constexpr int LDQ = D / 4 < 8 ? D / 4 : 8;           // lanes along d quads
-        constexpr int LAA = 32 / LDQ;                        // lanes along key quads
-        constexpr int GA = (BN / 4) / LAA;                   // lane groups along keys
-        constexpr int GD = (D / 4) / LDQ;                    // lane groups along d
-        constexpr int PER = GA * GD / 4;                     // groups per warp
-        static_assert(GA * GD % 4 == 0 && PER >= 1, "V transposer work split");
+        constexpr int LDQ = D / 4 < 8 ? D / 4 : 8;           // D = 16: lanes along d quads
+        constexpr int LAA = 32 / LDQ;                        // D = 16: lanes along key quads
+        constexpr int GA = (BN / 4) / LAA;                   // D = 16: lane groups along keys
+        constexpr int GD = (D / 4) / LDQ;                    // D = 16: lane groups along d
+        constexpr int PER = (BN / 4) * (D / 4) / 128;        // 4x4 blocks per thread per tile
+        static_assert((BN / 4) * (D / 4) % 128 == 0 && PER >= 1, "V transposer work split");
+        static_assert(D < 32 || (BN % 32 == 0 && D % 32 == 0), "diagonal transposer map");
         const int aa_lo = lane % LAA, dq_lo = lane / LAA;
+        // (key quad, d quad) of this thread's it-th block
+        auto blk = [&](int it, int& aa, int& dq) {
+            if constexpr (D >= 32) {
+                const int q = lane & 7;
+                const int c = it * 16 + wv * 4 + (lane >> 3);   // quarter-warp's (s, ah, dh)
+                const int rest = c >> 3;
+                aa = 8 * (rest % (BN / 32)) + q;
+                dq = 8 * (rest / (BN / 32)) + (q ^ (c & 7));
+            } else {
+                const int G = it * 4 + wv;
+                aa = (G % GA) * LAA + aa_lo;
+                dq = (G / GA) * LDQ + dq_lo;
+            }
+        };
         // Byte offset of V[key][d] in a TMA-staged tile (box {CH floats, BN keys} per
         // d chunk, swizzled: 16-byte chunk index XOR key bits).
         auto staged = [](int key, int dq) -> int {
@@ -539,9 +558,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 float4 x[PER][4];
 #pragma unroll
                 for (int it = 0; it < PER && loaded; ++it) {
-                    const int G = it * 4 + wv;
-                    const int aa = (G % GA) * LAA + aa_lo;
-                    const int dq = (G / GA) * LDQ + dq_lo;
+                    int aa, dq;
+                    blk(it, aa, dq);
 #pragma unroll
                     for (int rr = 0; rr < 4; ++rr)
                         x[it][rr] = *reinterpret_cast<const float4*>(vt + staged(aa * 4 + rr, dq));
@@ -549,7 +567,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 if (GUARD && kvalid < BN) {   // the sequence's last block (uniform over the CTA)
 #pragma unroll
                     for (int it = 0; it < PER; ++it) {
-                        const int aa = ((it * 4 + wv) % GA) * LAA + aa_lo;
+                        int aa, dq;
+                        blk(it, aa, dq);
 #pragma unroll
                         for (int rr = 0; rr < 4; ++rr)
                             if (aa * 4 + rr >= kvalid) x[it][rr] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -559,9 +578,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 if (named_barrier_or(2, 128, !loaded || *abort_flag)) { ok = false; break; }
 #pragma unroll
                 for (int it = 0; it < PER; ++it) {
-                    const int G = it * 4 + wv;
-                    const int aa = (G % GA) * LAA + aa_lo;
-                    const int dq = (G / GA) * LDQ + dq_lo;
+                    int aa, dq;
+                    blk(it, aa, dq);
                     const int kc = aa >> 3;                      // 32-key chunk of the V^T row
                     const float4 c0 = x[it][0], c1 = x[it][1], c2 = x[it][2], c3 = x[it][3];
                     const uint4 wr[4] = {
@@ -610,13 +628,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 tc_fence_after();
                 const uint32_t s_col = lane_base + kColS + (uint32_t)((gb % C::NSBUF) * C::S_BUF);
                 float s[BN];
+                {   // all chunks of the row in flight before one wait
+                    uint32_t wv[BN];
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t wv[32];
-                    tmem_ld32(s_col + 32 * c, wv);
+                    for (int c = 0; c < BN / 32; ++c)
+                        tmem_ld32(s_col + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(wv + 32 * c));
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(wv[e]);
+                    for (int e = 0; e < BN; ++e) s[e] = __uint_as_float(wv[e]);
                 }
                 const int k0 = j * BN;
                 const int nvis = min(max(key_lim - k0, 0), BN);     // visible keys of this block
