@@ -38,6 +38,16 @@ from resident_kv_cache_gb300 import inputs  # noqa: E402
 METRIC = "decode KV-read GB/s & prefill attention TFLOP/s, % of GB300 roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TF32_PER_BF16 = 1.1 / 2.25      # nominal dense TF32 : BF16 ratio
+NOMINAL = {"GB/s": 7900.0, "TFLOP/s": 1100.0}   # GB300 datasheet: HBM3e bandwidth, dense TF32
+
+
+def with_nominal(r):
+    """Add the datasheet fraction beside the measured one."""
+    peak = NOMINAL.get(r.get("unit"))
+    if peak and r.get("achieved", r.get("value")) is not None:
+        a = r.get("achieved", r.get("value"))
+        r["nominal"] = {"peak": peak, "frac": a / peak, "note": "datasheet: HBM3e 7.9 TB/s, dense TF32 1.1 PFLOP/s"}
+    return r
 PREFILL = inputs.CAUSAL_GQA
 DECODE = inputs.BATCHED_DECODE
 FILL_LEN = inputs.CAUSAL_GQA_CACHE_LEN
@@ -283,6 +293,8 @@ def run_rkv(args, rank, world, torch, dist):
                          "traffic": ncu_traffic("scatter"), "peak_note": f"{peak_kind} copy bandwidth",
                          "ms": fill_ms},
     }
+    for r in rooflines.values():
+        with_nominal(r)
     dominant = max(rooflines, key=lambda k: rooflines[k]["ms"])
     out = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -486,6 +498,7 @@ def measure_configs(torch, rkv, dev, stream, main, peaks, peak_kind):
     for v in out.values():
         v["peak_note"] = f"{peak_kind} " + ("copy bandwidth" if v["bound"] == "hbm" else
                                             "bf16 burst x nominal TF32/BF16 ratio 1.1/2.25")
+        with_nominal(v)
     return out, T
 
 
