@@ -62,7 +62,8 @@ class DecodeShape:
     extra: dict = field(default_factory=dict)
 
 
-# The five workloads (shapes as the task description states them).
+# The five workloads: a tiny MHA prefill, an encoder prefill, a causal GQA prefill with its cache
+# fill, a batched decode step and a long-context decode.
 TINY = PrefillShape("tiny non-causal MHA prefill S=32 H=2 D=16", 1, 32, 2, 2, 16, False)
 ENCODER = PrefillShape("encoder non-causal MHA prefill S=1500 H=8 D=64", 1, 1500, 8, 8, 64, False)
 CAUSAL_GQA = PrefillShape("causal GQA prefill B=4 S=2048 H=32 Hk=8 D=128", 4, 2048, 32, 8, 128, True)
