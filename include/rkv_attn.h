@@ -77,6 +77,19 @@ const char* rkv_last_error(void);
 rkv_status rkv_read_device_flags(unsigned int* flags, int clear, cudaStream_t stream);
 
 /*
+ * Self-check of the failure path of the on-chip waits.  Every mbarrier wait in
+ * the kernels is bounded (2 s per phase); on expiry the kernel sets
+ * RKV_FLAG_WAIT_TIMEOUT, unwinds (lets its copies and MMAs in flight finish,
+ * frees tensor memory) and returns, so the context stays usable.  This call
+ * runs the same bounded wait in one warp on a barrier that nothing completes,
+ * with a limit of limit_us microseconds: it must give up, set
+ * RKV_FLAG_WAIT_TIMEOUT and return.  limit_us in [1, 1000000]
+ * (RKV_ERR_INVALID_ARG otherwise).  Asynchronous on `stream`; read the flag
+ * with rkv_read_device_flags.
+ */
+rkv_status rkv_check_wait_timeout(unsigned int limit_us, cudaStream_t stream);
+
+/*
  * Prefill attention over interleaved activations, causal or not, with GQA.
  *
  * Cites: trueno-gpu attention.rs, fn batched_multihead_attention_optimized

@@ -63,6 +63,8 @@ def load():
     lib.rkv_last_error.argtypes = []
     lib.rkv_read_device_flags.restype = I
     lib.rkv_read_device_flags.argtypes = [ctypes.POINTER(ctypes.c_uint), I, P]
+    lib.rkv_check_wait_timeout.restype = I
+    lib.rkv_check_wait_timeout.argtypes = [ctypes.c_uint, P]
     lib.attn_prefill.restype = I
     lib.attn_prefill.argtypes = [P, P, P, P, I, I, I, I, I, I, P, F, P]
     lib.attn_prefill_fill_cache.restype = I
@@ -129,6 +131,11 @@ def rkv_read_device_flags(clear: bool = False, stream=None) -> int:
     _check("rkv_read_device_flags", load().rkv_read_device_flags(ctypes.byref(out), int(clear),
                                                                   _stream(stream)))
     return out.value
+
+
+def rkv_check_wait_timeout(limit_us: int, stream=None) -> None:
+    """Run the bounded on-chip wait on a barrier nothing completes (gives up after limit_us)."""
+    _check("rkv_check_wait_timeout", load().rkv_check_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def attn_prefill(q, k, v, o, batch, seq_len, n_heads, n_kv_heads, head_dim, causal,

@@ -135,6 +135,31 @@ rkv_status rkv_read_device_flags(unsigned int* flags, int clear, cudaStream_t st
     return RKV_OK;
 }
 
+// One warp waits, through the kernels' own bounded-wait helper, on a barrier whose first phase
+// nothing completes.
+__global__ void wait_check_kernel(uint64_t limit_ns, unsigned int* flags) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ volatile int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(&bar), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    (void)mbar_wait(smem_addr(&bar), 0u, &abort_flag, flags, limit_ns);
+}
+
+rkv_status rkv_check_wait_timeout(unsigned int limit_us, cudaStream_t stream) {
+    g_msg[0] = 0;
+    if (limit_us == 0u || limit_us > 1000000u)
+        return set_error(RKV_ERR_INVALID_ARG, "rkv_check_wait_timeout: limit_us must be in [1, 1000000], got %u",
+                         limit_us);
+    unsigned int* flags = device_flags_ptr();
+    if (!flags) return set_error(RKV_ERR_LAUNCH, "rkv_check_wait_timeout: no device flag word");
+    wait_check_kernel<<<1, 32, 0, stream>>>((uint64_t)limit_us * 1000ull, flags);
+    return check_launch("rkv_check_wait_timeout");
+}
+
 rkv_status attn_prefill(const float* q, const float* k, const float* v, float* o, int batch, int seq_len,
                         int n_heads, int n_kv_heads, int head_dim, int causal, const int* seq_lens,
                         float scale, cudaStream_t stream) {

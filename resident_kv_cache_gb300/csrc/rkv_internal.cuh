@@ -116,14 +116,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // *abort and the device timeout flag) if the limit expires, or false at once
 // if another thread of the CTA has already aborted.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          unsigned int* flags) {
+                                          unsigned int* flags, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 15u) == 0u) {
             if (*abort) return false;
-            if (global_ns() - t0 > kWaitLimitNs) {
+            if (global_ns() - t0 > limit_ns) {
                 *abort = 1;
                 atomicOr(flags, RKV_FLAG_WAIT_TIMEOUT);
                 return false;

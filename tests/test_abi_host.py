@@ -192,6 +192,12 @@ def test_decode_append_host_validation(lib):
     binding.attn_decode_append(None, None, None, None, None, None, 0, 32, 8, 128, 64, None, 0.0, None, 0, stream=0)
 
 
+def test_wait_check_host_validation(lib):
+    _expect(INV, binding.rkv_check_wait_timeout, 0, stream=0)           # no limit
+    _expect(INV, binding.rkv_check_wait_timeout, 1000001, stream=0)     # above 1 s
+    assert "limit_us" in binding.rkv_last_error()
+
+
 def test_last_error_is_per_call(lib):
     _expect(INV, binding.attn_prefill, A, A, A, A, 1, 8, 3, 2, 64, 1, stream=0)
     assert "multiple" in binding.rkv_last_error()
