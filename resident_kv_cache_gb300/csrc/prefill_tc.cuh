@@ -658,19 +658,46 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const float m_use = need ? m_blk : m_run;
                 const float alpha = need ? fast_exp2(m_run - m_blk) : 1.0f;
                 // p = 2^(s*c - m); the tensor core truncates f32 operands to TF32, so p is
-                // truncated here too and the row sum is taken over exactly those values
-                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                // truncated here too and the row sum is taken over exactly those values, in eight
+                // partial sums (column e into sum e & 7).
+                float ls[8];
+                if constexpr (BN == 64) {
+                    // Columns in pairs through the packed f32x2 FMA and add: the same per-lane
+                    // roundings as the scalar loop below, half the instructions on the softmax's
+                    // critical path (packed sum k holds partial sums 2k and 2k+1).
+                    uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
+                    const uint64_t sl2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-m_use, -m_use);
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t wv[32];
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t wv[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float x = s[32 * c + e];
-                        const float p = fast_exp2(fmaf(x, scale_log2, -m_use));   // 2^-inf = +0 when masked
-                        wv[e] = __float_as_uint(p) & 0xFFFFE000u;
-                        ls[e & 7] += __uint_as_float(wv[e]);
+                        for (int e = 0; e < 32; e += 2) {
+                            float t0, t1;
+                            f2_unpack(f2_fma(f2_pack(s[32 * c + e], s[32 * c + e + 1]), sl2, nm2), t0, t1);
+                            wv[e] = __float_as_uint(fast_exp2(t0)) & 0xFFFFE000u;   // 2^-inf = +0 when masked
+                            wv[e + 1] = __float_as_uint(fast_exp2(t1)) & 0xFFFFE000u;
+                            ls2[(e & 7) >> 1] =
+                                f2_add(ls2[(e & 7) >> 1], f2_pack(__uint_as_float(wv[e]), __uint_as_float(wv[e + 1])));
+                        }
+                        tmem_st32(s_col + 32 * c, wv);
                     }
-                    tmem_st32(s_col + 32 * c, wv);
+#pragma unroll
+                    for (int k2 = 0; k2 < 4; ++k2) f2_unpack(ls2[k2], ls[2 * k2], ls[2 * k2 + 1]);
+                } else {   // BN = 128: all 128 scores are live; the packed form would spill here
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ls[e] = 0.f;
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t wv[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const float x = s[32 * c + e];
+                            const float p = fast_exp2(fmaf(x, scale_log2, -m_use));   // 2^-inf = +0 when masked
+                            wv[e] = __float_as_uint(p) & 0xFFFFE000u;
+                            ls[e & 7] += __uint_as_float(wv[e]);
+                        }
+                        tmem_st32(s_col + 32 * c, wv);
+                    }
                 }
                 const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
                 l_run = l_run * alpha + lsum;
