@@ -310,9 +310,22 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
                     const int row = p * C::RPW + rgrp;
                     float4 kv = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (row < nvalid) kv = Ks[row * C::LPR + seg];
+                    if constexpr (G <= 4) {
+                        // q.k of the lane's four dims as two packed f32x2 products (x,y and z,w)
+                        // summed; at G = 8 the packed form needs more registers than it saves
+                        const uint64_t k01 = f2_pack(kv.x, kv.y), k23 = f2_pack(kv.z, kv.w);
 #pragma unroll
-                    for (int h = 0; h < G; ++h)
-                        part[p * G + h] = qv[h].x * kv.x + qv[h].y * kv.y + qv[h].z * kv.z + qv[h].w * kv.w;
+                        for (int h = 0; h < G; ++h) {
+                            float a, b;
+                            f2_unpack(f2_fma(f2_pack(qv[h].z, qv[h].w), k23, f2_mul(f2_pack(qv[h].x, qv[h].y), k01)),
+                                      a, b);
+                            part[p * G + h] = a + b;
+                        }
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < G; ++h)
+                            part[p * G + h] = qv[h].x * kv.x + qv[h].y * kv.y + qv[h].z * kv.z + qv[h].w * kv.w;
+                    }
                 }
                 xpose_reduce<C::NV, C::LPR>(part, lane);
                 // ---- scatter the totals to sc[row * G + h]
@@ -364,21 +377,39 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
                     const float a = __shfl_sync(0xffffffffu, alpha, h);
+                    if constexpr (G <= 4) {
+                        const uint64_t a2 = f2_pack(a, a);
+                        f2_unpack(f2_mul(f2_pack(acc[h][0], acc[h][1]), a2), acc[h][0], acc[h][1]);
+                        f2_unpack(f2_mul(f2_pack(acc[h][2], acc[h][3]), a2), acc[h][2], acc[h][3]);
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) acc[h][j] *= a;
+                        for (int j = 0; j < 4; ++j) acc[h][j] *= a;
+                    }
                 }
 #pragma unroll
                 for (int p = 0; p < C::PASSES; ++p) {
                     const int row = p * C::RPW + rgrp;
                     if (row < nvalid) {
                         const float4 vv = Vs[row * C::LPR + seg];
+                        if constexpr (G <= 4) {
+                            // acc += w * v, two dims per packed f32x2 FMA (per-lane rounding as fmaf)
+                            const uint64_t v01 = f2_pack(vv.x, vv.y), v23 = f2_pack(vv.z, vv.w);
 #pragma unroll
-                        for (int h = 0; h < G; ++h) {
-                            const float w = sc[row * G + h];
-                            acc[h][0] += w * vv.x;
-                            acc[h][1] += w * vv.y;
-                            acc[h][2] += w * vv.z;
-                            acc[h][3] += w * vv.w;
+                            for (int h = 0; h < G; ++h) {
+                                const float w = sc[row * G + h];
+                                const uint64_t w2 = f2_pack(w, w);
+                                f2_unpack(f2_fma(w2, v01, f2_pack(acc[h][0], acc[h][1])), acc[h][0], acc[h][1]);
+                                f2_unpack(f2_fma(w2, v23, f2_pack(acc[h][2], acc[h][3])), acc[h][2], acc[h][3]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int h = 0; h < G; ++h) {
+                                const float w = sc[row * G + h];
+                                acc[h][0] += w * vv.x;
+                                acc[h][1] += w * vv.y;
+                                acc[h][2] += w * vv.z;
+                                acc[h][3] += w * vv.w;
+                            }
                         }
                     }
                 }
