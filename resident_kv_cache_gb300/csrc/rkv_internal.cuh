@@ -40,21 +40,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// Round an f32 to the nearest TF32 value (ties away from zero), kept in an f32 container.
-__device__ __forceinline__ uint32_t round_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
-// Round an f32 to the nearest TF32 value (ties away from zero) with integer ops:
-// add half a TF32 ulp to the magnitude bits and clear the 13 low mantissa bits.
-// Inf and NaN are passed through unchanged.
-__device__ __forceinline__ uint32_t round_tf32_int(float x) {
-    const uint32_t u = __float_as_uint(x);
-    return (u & 0x7FFFFFFFu) < 0x7F800000u ? ((u + 0x1000u) & 0xFFFFE000u) : u;
-}
-
 // Named barrier over `nthreads` threads that also ORs `pred` across them: every thread
 // gets the same answer, so a group can take an exit decision together.
 __device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t nthreads, bool pred) {
@@ -142,18 +127,8 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint64
 }
 
 // ------------------------------------------------------------ bulk / TMA copy
-// Contiguous global -> shared copy completing on an mbarrier (16-byte aligned,
-// size a multiple of 16).
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-// Same, with an L2 cache policy (from l2_policy_evict_first) for data read once.
+// Contiguous global -> shared copy completing on an mbarrier (16-byte aligned, size a multiple
+// of 16), with an L2 cache policy (from l2_policy_evict_first) for data read once.
 __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
                                               uint64_t policy) {
     asm volatile(
@@ -258,16 +233,6 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool b_mn_major) {
     return (1u << 4) | (2u << 7) | (2u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-// D[tmem] (+)= A[smem desc] * B[smem desc]   (kind::tf32, one CTA)
-__device__ __forceinline__ void mma_tf32_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
 }
 
 // D[tmem] (+)= A[tmem] * B[smem desc]   (kind::tf32, one CTA)
