@@ -22,6 +22,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -130,10 +131,16 @@ class ClockSampler:
 
 
 def kernel_hash(*files):
+    """Hash of a kernel's source code with comments and blank lines removed, so that counters
+    taken on a kernel stay attached to it until its code (not its commentary) changes."""
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "resident_kv_cache_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "resident_kv_cache_gb300", "csrc", f), encoding="utf-8") as fh:
+            text = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
+        for line in text.splitlines():
+            line = re.sub(r"//.*$", "", line).rstrip()
+            if line.strip():
+                h.update(line.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -20,10 +20,15 @@
 //    read from HBM once per kv head.  Dot products are split over D/4 lanes and
 //    reduced with a transposing butterfly (one shuffle per partial, not one per
 //    head per step); the softmax is online in base 2 with the scale folded into q.
+//    For G <= 4 the products and the P.V accumulation run as packed f32x2 FMAs.
 //  * Each piece ends with (m, l, o) per head.  A piece that is a whole segment
 //    writes the output directly; otherwise it writes a partial record to the
 //    workspace, and the last CTA to finish a segment (atomic ticket) merges the
-//    records with the log-sum-exp rule and resets the ticket to zero.
+//    records with the log-sum-exp rule, one warp per query head, and resets the
+//    ticket to zero.
+//  * With k_new / v_new (the one-launch decode step), the CTA whose share holds
+//    row len-1 of a segment first writes the new row there, then fences it
+//    before its own bulk copies read it.
 #include "rkv_internal.cuh"
 #include "rkv_launch.h"
 
