@@ -15,9 +15,9 @@
 //    segment boundaries, and each part of a segment in one CTA is a "piece".
 //  * A producer warp streams tiles of K and V (8 rows per consumer warp) with bulk
 //    async copies into a 2-4 stage shared-memory ring (mbarrier full/empty pairs).
-//  * Twelve consumer warps (eight for G = 8) each take 8 rows of a tile.  GQA: the G = H/Hk query
-//    heads that share a kv head are processed together, so every cache row is
-//    read from HBM once per kv head.  Dot products are split over D/4 lanes and
+//  * Eleven or twelve consumer warps (eight for G = 8) each take 8 rows of a tile.  GQA: the
+//    G = H/Hk query heads that share a kv head are processed together, so every cache row
+//    is read from HBM once per kv head.  Dot products are split over the lanes of a row and
 //    reduced with a transposing butterfly (one shuffle per partial, not one per
 //    head per step); the softmax is online in base 2 with the scale folded into q.
 //    For G <= 4 the products and the P.V accumulation run as packed f32x2 FMAs.
@@ -42,13 +42,18 @@ __host__ __device__ constexpr int ilog2c(int x) { return x <= 1 ? 0 : 1 + ilog2c
 
 template <int D, int G>
 struct DecCfg {
-    // Consumer warps: 12 (four per SM sub-partition, <= 128 registers each) hide the
-    // shared-memory and shuffle latencies better than 8; G = 8 needs more registers.
-    static constexpr int W = G <= 4 ? 12 : 8;
+    // Consumer warps: 11 or 12 hide the shared-memory and shuffle latencies better than 8;
+    // G = 8 needs more registers.
+    // FPL float4 columns of a row per lane: 2 for D >= 64 at G <= 4 halves the butterfly that
+    // sums the partial dot products; the extra q and accumulator registers need the 170 a
+    // thread gets with 12 warps per CTA (3 per sub-partition), so 11 consumer warps there.
+    static constexpr int FPL = (G <= 4 && D >= 64) ? 2 : 1;
+    static constexpr int W = FPL == 2 ? 11 : (G <= 4 ? 12 : 8);
     static constexpr int CT = W * 32;                 // consumer threads
     static constexpr int THREADS = CT + 32;           // + one producer warp
     static constexpr int TILE_ROWS = kDecBatchRows * W;
-    static constexpr int LPR = D / 4;                 // lanes per cache row (one float4 each)
+    static constexpr int D4 = D / 4;                  // float4 per cache row
+    static constexpr int LPR = D4 / FPL;              // lanes per cache row
     static constexpr int RPW = 32 / LPR;              // rows a warp covers per pass
     static constexpr int PASSES = kDecBatchRows / RPW;
     static constexpr int NV = PASSES * G;             // partial dot products per lane
@@ -274,8 +279,8 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
     const int rgrp = lane / C::LPR;        // row group within a pass
     float* sc = sc_all + warp * C::ENTRIES;
 
-    float4 qv[G];
-    float acc[G][4];
+    float4 qv[G][C::FPL];
+    float acc[G][4 * C::FPL];
     float m_run = -INFINITY, l_run = 0.0f;
     bool ok = true;
     int it = 0;
@@ -289,10 +294,14 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
         // q of the G heads sharing kv head kh, pre-scaled so scores are in log2 units
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            float4 t = __ldg(reinterpret_cast<const float4*>(q + (int64_t)m * H * D + (int64_t)(kh * G + h) * D) + seg);
-            qv[h] = make_float4(t.x * scale_log2, t.y * scale_log2, t.z * scale_log2, t.w * scale_log2);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[h][j] = 0.0f;
+            for (int f = 0; f < C::FPL; ++f) {
+                float4 t = __ldg(reinterpret_cast<const float4*>(q + (int64_t)m * H * D + (int64_t)(kh * G + h) * D) +
+                                 seg + f * C::LPR);
+                qv[h][f] = make_float4(t.x * scale_log2, t.y * scale_log2, t.z * scale_log2, t.w * scale_log2);
+            }
+#pragma unroll
+            for (int j = 0; j < 4 * C::FPL; ++j) acc[h][j] = 0.0f;
         }
         m_run = -INFINITY;
         l_run = 0.0f;
@@ -305,31 +314,44 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
             const int nvalid = min(max(tile_rows - warp * kDecBatchRows, 0), kDecBatchRows);
             if (ok && nvalid > 0) {
                 const float4* Ks = reinterpret_cast<const float4*>(smem + C::OFF_STAGES + (2 * s) * C::TILE_BYTES) +
-                                   (warp * kDecBatchRows) * C::LPR;
+                                   (warp * kDecBatchRows) * C::D4;
                 const float4* Vs = reinterpret_cast<const float4*>(smem + C::OFF_STAGES + (2 * s + 1) * C::TILE_BYTES) +
-                                   (warp * kDecBatchRows) * C::LPR;
+                                   (warp * kDecBatchRows) * C::D4;
                 // ---- partial dot products: pass p covers rows p*RPW .. p*RPW+RPW-1
                 float part[C::NV];
 #pragma unroll
                 for (int p = 0; p < C::PASSES; ++p) {
                     const int row = p * C::RPW + rgrp;
-                    float4 kv = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (row < nvalid) kv = Ks[row * C::LPR + seg];
+                    float4 kv[C::FPL];
+#pragma unroll
+                    for (int f = 0; f < C::FPL; ++f)
+                        kv[f] = row < nvalid ? Ks[row * C::D4 + seg + f * C::LPR] : make_float4(0.f, 0.f, 0.f, 0.f);
                     if constexpr (G <= 4) {
-                        // q.k of the lane's four dims as two packed f32x2 products (x,y and z,w)
-                        // summed; at G = 8 the packed form needs more registers than it saves
-                        const uint64_t k01 = f2_pack(kv.x, kv.y), k23 = f2_pack(kv.z, kv.w);
+                        // q.k of the lane's dims as packed f32x2 products (x,y and z,w lanes) summed;
+                        // at G = 8 the packed form needs more registers than it saves
 #pragma unroll
                         for (int h = 0; h < G; ++h) {
+                            uint64_t t = f2_mul(f2_pack(qv[h][0].x, qv[h][0].y), f2_pack(kv[0].x, kv[0].y));
+                            t = f2_fma(f2_pack(qv[h][0].z, qv[h][0].w), f2_pack(kv[0].z, kv[0].w), t);
+#pragma unroll
+                            for (int f = 1; f < C::FPL; ++f) {
+                                t = f2_fma(f2_pack(qv[h][f].x, qv[h][f].y), f2_pack(kv[f].x, kv[f].y), t);
+                                t = f2_fma(f2_pack(qv[h][f].z, qv[h][f].w), f2_pack(kv[f].z, kv[f].w), t);
+                            }
                             float a, b;
-                            f2_unpack(f2_fma(f2_pack(qv[h].z, qv[h].w), k23, f2_mul(f2_pack(qv[h].x, qv[h].y), k01)),
-                                      a, b);
+                            f2_unpack(t, a, b);
                             part[p * G + h] = a + b;
                         }
                     } else {
 #pragma unroll
-                        for (int h = 0; h < G; ++h)
-                            part[p * G + h] = qv[h].x * kv.x + qv[h].y * kv.y + qv[h].z * kv.z + qv[h].w * kv.w;
+                        for (int h = 0; h < G; ++h) {
+                            float t = 0.0f;
+#pragma unroll
+                            for (int f = 0; f < C::FPL; ++f)
+                                t += qv[h][f].x * kv[f].x + qv[h][f].y * kv[f].y + qv[h][f].z * kv[f].z +
+                                     qv[h][f].w * kv[f].w;
+                            part[p * G + h] = t;
+                        }
                     }
                 }
                 xpose_reduce<C::NV, C::LPR>(part, lane);
@@ -384,36 +406,45 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
                     const float a = __shfl_sync(0xffffffffu, alpha, h);
                     if constexpr (G <= 4) {
                         const uint64_t a2 = f2_pack(a, a);
-                        f2_unpack(f2_mul(f2_pack(acc[h][0], acc[h][1]), a2), acc[h][0], acc[h][1]);
-                        f2_unpack(f2_mul(f2_pack(acc[h][2], acc[h][3]), a2), acc[h][2], acc[h][3]);
+#pragma unroll
+                        for (int j = 0; j < 4 * C::FPL; j += 2)
+                            f2_unpack(f2_mul(f2_pack(acc[h][j], acc[h][j + 1]), a2), acc[h][j], acc[h][j + 1]);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) acc[h][j] *= a;
+                        for (int j = 0; j < 4 * C::FPL; ++j) acc[h][j] *= a;
                     }
                 }
 #pragma unroll
                 for (int p = 0; p < C::PASSES; ++p) {
                     const int row = p * C::RPW + rgrp;
                     if (row < nvalid) {
-                        const float4 vv = Vs[row * C::LPR + seg];
+                        float4 vv[C::FPL];
+#pragma unroll
+                        for (int f = 0; f < C::FPL; ++f) vv[f] = Vs[row * C::D4 + seg + f * C::LPR];
                         if constexpr (G <= 4) {
                             // acc += w * v, two dims per packed f32x2 FMA (per-lane rounding as fmaf)
-                            const uint64_t v01 = f2_pack(vv.x, vv.y), v23 = f2_pack(vv.z, vv.w);
 #pragma unroll
                             for (int h = 0; h < G; ++h) {
                                 const float w = sc[row * G + h];
                                 const uint64_t w2 = f2_pack(w, w);
-                                f2_unpack(f2_fma(w2, v01, f2_pack(acc[h][0], acc[h][1])), acc[h][0], acc[h][1]);
-                                f2_unpack(f2_fma(w2, v23, f2_pack(acc[h][2], acc[h][3])), acc[h][2], acc[h][3]);
+#pragma unroll
+                                for (int f = 0; f < C::FPL; ++f) {
+                                    float* a4 = acc[h] + 4 * f;
+                                    f2_unpack(f2_fma(w2, f2_pack(vv[f].x, vv[f].y), f2_pack(a4[0], a4[1])), a4[0], a4[1]);
+                                    f2_unpack(f2_fma(w2, f2_pack(vv[f].z, vv[f].w), f2_pack(a4[2], a4[3])), a4[2], a4[3]);
+                                }
                             }
                         } else {
 #pragma unroll
                             for (int h = 0; h < G; ++h) {
                                 const float w = sc[row * G + h];
-                                acc[h][0] += w * vv.x;
-                                acc[h][1] += w * vv.y;
-                                acc[h][2] += w * vv.z;
-                                acc[h][3] += w * vv.w;
+#pragma unroll
+                                for (int f = 0; f < C::FPL; ++f) {
+                                    acc[h][4 * f + 0] += w * vv[f].x;
+                                    acc[h][4 * f + 1] += w * vv[f].y;
+                                    acc[h][4 * f + 2] += w * vv[f].z;
+                                    acc[h][4 * f + 3] += w * vv[f].w;
+                                }
                             }
                         }
                     }
@@ -431,12 +462,14 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
 #pragma unroll
             for (int h = 0; h < G; ++h)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[h][j] += __shfl_xor_sync(0xffffffffu, acc[h][j], o);
+                for (int j = 0; j < 4 * C::FPL; ++j) acc[h][j] += __shfl_xor_sync(0xffffffffu, acc[h][j], o);
         if (lane < C::LPR) {
 #pragma unroll
             for (int h = 0; h < G; ++h)
-                *reinterpret_cast<float4*>(red_acc + (warp * G + h) * D + seg * 4) =
-                    make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+#pragma unroll
+                for (int f = 0; f < C::FPL; ++f)
+                    *reinterpret_cast<float4*>(red_acc + (warp * G + h) * D + (seg + f * C::LPR) * 4) =
+                        make_float4(acc[h][4 * f], acc[h][4 * f + 1], acc[h][4 * f + 2], acc[h][4 * f + 3]);
         }
         if (lane < G) {
             red_ml[(warp * G + lane) * 2 + 0] = m_run;
