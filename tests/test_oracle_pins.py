@@ -292,6 +292,24 @@ def test_padded_query_rows_are_zero(oracle_mod):
     assert np.max(np.abs(o[0, :4] - o4[0])) < 1e-12
 
 
+def test_all_empty_batches_give_zero_rows(oracle_mod):
+    """Reading O3/O7 for a batch with no valid row at all (the decode has nothing to attend,
+    the prefill and the chunked prefill no valid query): every output row is exactly zero."""
+    M, H, Hk, D, L = 3, 4, 2, 8, 5
+    q = inputs.normal((M, H * D), (82, 0))
+    kc, vc = inputs.normal((M, Hk, L, D), (82, 1)), inputs.normal((M, Hk, L, D), (82, 2))
+    assert np.all(oracle_mod.decode(q, kc, vc, M, H, Hk, D, L, np.zeros(M, np.int32)) == 0)
+    B, S = 2, 6
+    qp, kp, vp = (inputs.normal((B, S, n * D), (83, t)) for t, n in enumerate((H, Hk, Hk)))
+    for causal in (False, True):
+        assert np.all(oracle_mod.prefill(qp, kp, vp, B, S, H, Hk, D, causal, seq_lens=np.zeros(B)) == 0)
+    qc = inputs.normal((B, 3, H * D), (84, 0))
+    kc2, vc2 = inputs.normal((B, Hk, 10, D), (84, 1)), inputs.normal((B, Hk, 10, D), (84, 2))
+    got = oracle_mod.prefill_cached(qc, kc2, vc2, B, 3, H, Hk, D, 10, True, np.array([0, 5], np.int32),
+                                    q_lens=np.zeros(B, np.int32))
+    assert np.all(got == 0)
+
+
 def test_prefill_rows_matches_full(oracle_mod):
     B, S, H, Hk, D = 2, 9, 4, 2, 8
     q, k, v = (inputs.normal((B, S, n * D), (91, t)) for t, n in enumerate((H, Hk, Hk)))
