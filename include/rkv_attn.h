@@ -59,6 +59,11 @@ typedef enum {
 #define RKV_FLAG_BAD_POINTER     0x8u  /* a per-sequence cache pointer was NULL or not 16-byte aligned: that
                                           sequence was skipped (no row read or written, zero output) */
 
+/* Bytes at the head of a decode workspace that hold its completion tickets
+ * (attn_decode_batched and the other decode entry points).  Their place does
+ * not depend on the call's sizes. */
+#define RKV_DECODE_TICKET_BYTES 32768
+
 /* Library version, (major << 16) | minor. */
 int rkv_version(void);
 
@@ -174,8 +179,10 @@ rkv_status attn_prefill_chunked(const float* q, const float* k_cache, const floa
                                 const int* q_lens, float scale, cudaStream_t stream);
 
 /*
- * Bytes of device workspace attn_decode_batched needs for these sizes.
- * Returns 0 for invalid sizes.
+ * Bytes of device workspace attn_decode_batched needs for these sizes:
+ * RKV_DECODE_TICKET_BYTES of tickets, then the split-KV partial records.
+ * Returns 0 for invalid sizes (including M * n_kv_heads above
+ * RKV_DECODE_TICKET_BYTES / 4).
  */
 size_t attn_decode_workspace_bytes(int M, int n_heads, int n_kv_heads, int head_dim,
                                    int max_len);
@@ -198,11 +205,18 @@ size_t attn_decode_workspace_bytes(int M, int n_heads, int n_kv_heads, int head_
  *              (the length INCLUDING the token just appended).  len > max_len
  *              is clamped (RKV_FLAG_LEN_CLAMPED); len <= 0 gives a zero row.
  *   workspace  device buffer of >= attn_decode_workspace_bytes(...) bytes,
- *              256-byte aligned, ZERO-FILLED before its first use; every call
- *              leaves the parts that must start at zero zeroed again, so it can
- *              be reused without clearing.  Calls sharing one workspace must
- *              not overlap on the GPU (use one workspace per concurrent stream).
- * 1 <= M <= 32; n_heads / n_kv_heads in {1, 2, 4, 8}.  Split-KV: the cache rows
+ *              256-byte aligned, ZERO-FILLED before its first use.  Its first
+ *              RKV_DECODE_TICKET_BYTES bytes are completion tickets, one per
+ *              (sequence m, kv head kh) at int index m * n_kv_heads + kh,
+ *              whatever the sizes; every call that completes leaves them zero,
+ *              so one workspace sized for the largest call can be reused by
+ *              calls of any sizes without clearing.  A call that raised
+ *              RKV_FLAG_WAIT_TIMEOUT may leave tickets non-zero: zero the first
+ *              RKV_DECODE_TICKET_BYTES bytes before the workspace is used again.
+ *              Calls sharing one workspace must not overlap on the GPU (use one
+ *              workspace per concurrent stream).
+ * 1 <= M <= 32; n_heads / n_kv_heads in {1, 2, 4, 8}; M * n_kv_heads <=
+ * RKV_DECODE_TICKET_BYTES / 4 (RKV_ERR_UNSUPPORTED otherwise).  Split-KV: the cache rows
  * of all sequences are cut into equal contiguous pieces, one per CTA; pieces
  * of one (sequence, kv head) are merged with a log-sum-exp combine inside the
  * same launch.  Arithmetic is f32.
@@ -224,8 +238,10 @@ rkv_status attn_decode_batched(const float* q, const float* k_cache, const float
  * memory, held on every GPU that loads the library until the process exits;
  * sizes whose workspace (attn_decode_workspace_bytes) exceeds it are rejected
  * with RKV_ERR_UNSUPPORTED.  Nothing is allocated: no cudaMalloc, no library
- * allocator.  The first call on a device looks up the array's device address
- * (make it before any stream capture).  Each call clears the part of the
+ * allocator.  The first call on a device looks up the array's device address,
+ * and so does the first call after that device's context changed (for
+ * instance after cudaDeviceReset); make the first call before any stream
+ * capture.  The lookup is guarded by a lock.  Each call clears the part of the
  * array that must start at zero with an asynchronous memset on `stream`.
  * All calls share the one array: calls that overlap on the GPU (different
  * streams or host threads on one device) race and give wrong results.

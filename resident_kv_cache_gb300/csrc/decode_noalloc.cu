@@ -9,11 +9,16 @@
 // library's own device memory instead of a caller buffer.
 //
 // The array lives as long as the library is loaded, on every GPU that loads
-// it.  Its device address is looked up once per device, on the first call made
-// with that device current; make that first call before any stream capture.
-// Every call shares the one array: calls that overlap on the GPU (two streams,
-// or two host threads on one device) race on it and give wrong results.
+// it.  Its device address is looked up on the first call made with a device
+// current, and again whenever that device's context has changed since (for
+// instance after cudaDeviceReset); make that first call before any stream
+// capture.  Every call shares the one array: calls that overlap on the GPU
+// (two streams, or two host threads on one device) race on it and give wrong
+// results.
+#include <cuda.h>
+
 #include <cstdint>
+#include <mutex>
 
 #include "rkv_internal.cuh"
 #include "rkv_launch.h"
@@ -25,27 +30,63 @@ constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
 
-// Device address of g_decode_scratch for the current device (nullptr on failure).
+// Unique id of the current context (0 if none or unknown).  Ids are never reused within a
+// process, unlike context handles, so a context created after a reset never matches an old entry.
+static unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of g_decode_scratch for the current device (nullptr on failure), cached
+// per device together with the id of the context it was resolved in.
 static void* scratch_device_address(cudaError_t* err) {
     constexpr int kMaxDevices = 64;
-    static void* cached[kMaxDevices] = {nullptr};
+    struct Entry {
+        unsigned long long ctx_id;
+        void* ptr;
+    };
+    static Entry cached[kMaxDevices] = {};
+    static std::mutex mu;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         *err = e != cudaSuccess ? e : cudaErrorInvalidDevice;
         return nullptr;
     }
-    if (!cached[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_decode_scratch);
-        if (e != cudaSuccess) {
-            *err = e;
-            return nullptr;
-        }
-        cached[dev] = p;
+    std::lock_guard<std::mutex> lock(mu);
+    const unsigned long long id = current_context_id();
+    if (id != 0 && cached[dev].ptr && cached[dev].ctx_id == id) {
+        *err = cudaSuccess;
+        return cached[dev].ptr;
     }
+    void* p = nullptr;   // resolving also makes the device's primary context current
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) {
+        *err = e;
+        return nullptr;
+    }
+    cached[dev] = Entry{current_context_id(), p};
     *err = cudaSuccess;
-    return cached[dev];
+    return p;
 }
 
 }  // namespace rkv

@@ -582,11 +582,9 @@ static int rec_floats_rt(int D, int G) {
     return ((G * D + 2 * G) + 3) / 4 * 4;
 }
 
-static size_t tickets_bytes(int M, int Hk) { return ((size_t)M * Hk * 4 + 255) / 256 * 256; }
-
 size_t decode_workspace_bytes(int M, int H, int Hk, int D) {
     const int G = H / Hk;
-    return tickets_bytes(M, Hk) + (size_t)(M * Hk + kDecMaxCtas) * rec_floats_rt(D, G) * 4;
+    return (size_t)RKV_DECODE_TICKET_BYTES + (size_t)(M * Hk + kDecMaxCtas) * rec_floats_rt(D, G) * 4;
 }
 
 template <int D, int G>
@@ -606,7 +604,7 @@ static rkv_status launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
     if (n <= 0) return set_error(RKV_ERR_LAUNCH, "attn_decode_batched: cannot query the SM count");
     if (n > kDecMaxCtas) n = kDecMaxCtas;
     int* tickets = static_cast<int*>(a.workspace);
-    float* records = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + tickets_bytes(a.M, a.Hk));
+    float* records = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + RKV_DECODE_TICKET_BYTES);
     kern<<<n, C::THREADS, C::SMEM, stream>>>(a.q, a.k_cache, a.v_cache, a.k_ptrs, a.v_ptrs, a.o, a.M, a.Hk, a.Lmax,
                                                a.seq_lens, a.scale * kLog2e, tickets, records, a.flags, a.k_new,
                                                a.v_new);

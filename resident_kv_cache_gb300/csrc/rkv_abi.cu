@@ -269,7 +269,7 @@ rkv_status attn_prefill_chunked(const float* q, const float* k_cache, const floa
 
 size_t attn_decode_workspace_bytes(int M, int n_heads, int n_kv_heads, int head_dim, int max_len) {
     if (M <= 0 || M > kDecodeMaxSeqs || n_heads <= 0 || n_kv_heads <= 0 || max_len <= 0 ||
-        n_heads % n_kv_heads != 0 || !head_dim_supported(head_dim))
+        n_heads % n_kv_heads != 0 || !head_dim_supported(head_dim) || (int64_t)M * n_kv_heads > kDecodeTicketSlots)
         return 0;
     return decode_workspace_bytes(M, n_heads, n_kv_heads, head_dim);
 }
@@ -293,6 +293,9 @@ static rkv_status decode_entry(const char* op, const float* q, const float* k_ca
     if (!decode_group_supported(n_heads / n_kv_heads))
         return set_error(RKV_ERR_UNSUPPORTED, "%s: n_heads/n_kv_heads = %d not supported (1, 2, 4 or 8)", op,
                          n_heads / n_kv_heads);
+    if ((int64_t)M * n_kv_heads > kDecodeTicketSlots)
+        return set_error(RKV_ERR_UNSUPPORTED, "%s: M * n_kv_heads = %lld exceeds the %d workspace tickets", op,
+                         (long long)M * n_kv_heads, kDecodeTicketSlots);
     const bool ptrs = k_ptrs || v_ptrs;
     if (!q || !o || !seq_lens || !workspace || (ptrs ? (!k_ptrs || !v_ptrs) : (!k_cache || !v_cache)))
         return set_error(RKV_ERR_INVALID_ARG, "%s: q, caches, o, seq_lens and workspace must be non-NULL", op);

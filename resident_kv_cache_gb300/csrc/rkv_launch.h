@@ -11,6 +11,13 @@ namespace rkv {
 // cache_from_cache_from_kv_cache.rs, fn init_batched_kv_cache_gpu).
 constexpr int kDecodeMaxSeqs = 32;
 
+// The decode workspace starts with a fixed block of completion tickets, one int per
+// (sequence, kv head) at index m * n_kv_heads + kh, whatever the call's sizes; the partial
+// records follow it.  A workspace sized for the largest call therefore serves calls of any
+// sizes without clearing (each call leaves its tickets zero).
+constexpr int kDecodeTicketSlots = RKV_DECODE_TICKET_BYTES / 4;
+static_assert(RKV_DECODE_TICKET_BYTES % 256 == 0, "records start 256-byte aligned");
+
 struct PrefillArgs {
     const float* q;
     const float* k;        // interleaved [B, S, Hk*D], or the cache [B, Hk, max_len, D] (kv_cache)

@@ -100,6 +100,30 @@ def test_decode_workspace_query(lib):
     # grows with the record size
     assert binding.attn_decode_workspace_bytes(4, 32, 8, 64, 4096) < \
         binding.attn_decode_workspace_bytes(4, 32, 8, 128, 4096)
+    # the tickets take a fixed block at the head, whatever the sizes; the records grow with M * n_kv_heads
+    tb = binding.RKV_DECODE_TICKET_BYTES
+    assert binding.attn_decode_workspace_bytes(1, 8, 8, 16, 1) > tb
+    a8 = binding.attn_decode_workspace_bytes(8, 32, 8, 128, 4096)
+    a16 = binding.attn_decode_workspace_bytes(16, 32, 8, 128, 4096)
+    assert (a16 - tb) - (a8 - tb) == 8 * 8 * (4 * 128 + 2 * 4) * 4
+    # at most RKV_DECODE_TICKET_BYTES / 4 (sequence, kv head) pairs
+    assert binding.attn_decode_workspace_bytes(32, 256, 256, 16, 64) > 0
+    assert binding.attn_decode_workspace_bytes(32, 257, 257, 16, 64) == 0
+    assert binding.attn_decode_workspace_bytes(1, 8192, 8192, 16, 64) > 0
+    assert binding.attn_decode_workspace_bytes(1, 8193, 8193, 16, 64) == 0
+
+
+def test_ticket_block_size_matches_the_header():
+    import os
+    import re
+    hdr = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "rkv_attn.h")
+    m = re.search(r"#define\s+RKV_DECODE_TICKET_BYTES\s+(\d+)", open(hdr).read())
+    assert m and int(m.group(1)) == binding.RKV_DECODE_TICKET_BYTES
+
+
+def test_decode_rejects_more_pairs_than_tickets(lib):
+    # 32 sequences x 257 kv heads: more (sequence, kv head) pairs than the ticket block holds
+    _expect(UNS, binding.attn_decode_batched, A, A, A, A, 32, 257, 257, 16, 64, A, 0.0, A, 1 << 40, stream=0)
 
 
 @pytest.mark.parametrize("args,status", [

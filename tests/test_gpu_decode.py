@@ -93,9 +93,31 @@ def test_workspace_reuse_and_tickets_reset(rkv, oracle_mod):
     o1, ws = _decode(rkv, torch, q, kc, vc, M, H, Hk, D, L, lens)
     o2, _ = _decode(rkv, torch, q, kc, vc, M, H, Hk, D, L, lens, ws=ws)
     assert np.array_equal(o1, o2)
-    assert int(ws[0][: M * Hk * 4].view(torch.int32).abs().sum().item()) == 0
+    assert int(ws[0][: rkv.RKV_DECODE_TICKET_BYTES].view(torch.int32).abs().sum().item()) == 0
     want = oracle_mod.decode(q, kc, vc, M, H, Hk, D, L, np.array(lens))
     assert_close(o1, want, TOL)
+
+
+def test_one_workspace_serves_calls_of_different_sizes(rkv, oracle_mod):
+    """A workspace sized for the largest call, zero-filled once, reused by calls whose
+    (M, n_kv_heads) differ: the tickets sit at fixed places at its head, so a larger call's
+    tickets never land on a smaller call's records.  Lengths are long enough that every
+    (sequence, kv head) is split over several CTAs and merged through its ticket."""
+    torch = torch_cuda()
+    H, D, L = 32, 128, 4096
+    shapes = [(8, 8), (16, 8), (8, 8), (4, 16), (16, 8), (2, 32)]   # (M, Hk)
+    n = max(rkv.attn_decode_workspace_bytes(M, H, Hk, D, L) for M, Hk in shapes)
+    ws = (torch.zeros(n, dtype=torch.uint8, device="cuda"), n)
+    for i, (M, Hk) in enumerate(shapes):
+        lens = [4096 - 37 * m for m in range(M)]
+        q = inputs.normal((M, H * D), (900 + i, 0))
+        kc, vc = inputs.normal((M, Hk, L, D), (900 + i, 1)), inputs.normal((M, Hk, L, D), (900 + i, 2))
+        got, _ = _decode(rkv, torch, q, kc, vc, M, H, Hk, D, L, lens, ws=ws)
+        want = oracle_mod.decode(q, kc, vc, M, H, Hk, D, L, np.array(lens))
+        assert_close(got, want, TOL, what=f"call {i}: M={M}, Hk={Hk}")
+        tickets = ws[0][: rkv.RKV_DECODE_TICKET_BYTES].view(torch.int32)
+        assert int(tickets.abs().sum().item()) == 0, f"call {i} left a ticket set"
+    assert rkv.rkv_read_device_flags(clear=True) == 0
 
 
 def test_batched_decode_step_full_size(rkv, oracle_mod):

@@ -31,7 +31,9 @@ def _inputs(torch, M, H, Hk, D, L, lens, seed):
     (3, 8, 2, 64, 700, [700, 1, 333]),
     (2, 4, 4, 16, 50, [0, 50]),
 ])
-def test_noalloc_matches_workspace_entry_point_twice(rkv, M, H, Hk, D, L, lens):
+def test_noalloc_matches_workspace_entry_point_twice(rkv, oracle_mod, M, H, Hk, D, L, lens):
+    """Same kernel, same arithmetic, same split of the rows: the output must equal
+    attn_decode_batched's bit for bit, on both calls, and match the oracle."""
     torch = torch_cuda()
     if lens is None:
         lens = inputs.uniform_lengths(M, 1, L, inputs.SEED_LEN)
@@ -40,11 +42,16 @@ def test_noalloc_matches_workspace_entry_point_twice(rkv, M, H, Hk, D, L, lens):
     ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
     ref = torch.empty((M, H * D), device="cuda")
     rkv.attn_decode_batched(q, kc, vc, ref, M, H, Hk, D, L, ln, 0.0, ws, n)
+    torch.cuda.synchronize()
+    want = oracle_mod.decode(q.cpu().numpy(), kc.cpu().numpy(), vc.cpu().numpy(), M, H, Hk, D, L,
+                             np.asarray(lens, np.int32))
     for call in range(2):
         out = torch.full((M, H * D), float("nan"), device="cuda")
         rkv.attn_decode_batched_noalloc(q, kc, vc, out, M, H, Hk, D, L, ln, 0.0)
         torch.cuda.synchronize()
-        assert_close(out.cpu().numpy(), ref.cpu().numpy(), TOL, what=f"call {call}")
+        assert torch.equal(out, ref), f"call {call}: differs from attn_decode_batched"
+        assert_close(out.cpu().numpy(), want, TOL, what=f"call {call} against the oracle")
+    assert rkv.rkv_read_device_flags(clear=True) == 0
 
 
 @pytest.mark.gpu
