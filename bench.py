@@ -2,8 +2,10 @@
 """Benchmark of the resident-attention hot path on GB300.
 
 One step is one pass over every operation of the path:
-  1. causal GQA prefill   B=4, S=2048, H=32, Hk=8, D=128   (attn_prefill)
-  2. cache fill           its K/V scattered into a [4,8,4096,128] cache (kv_cache_scatter)
+  1. cache fill           the causal GQA sequences' K/V scattered into a [4,8,4096,128] cache
+                          (kv_cache_scatter; it needs only K and V, so it goes first and its
+                          dirty cache lines drain during the tensor-bound prefill)
+  2. causal GQA prefill   B=4, S=2048, H=32, Hk=8, D=128   (attn_prefill)
   3. batched decode step  M=32, H=32, Hk=8, D=128, cache [32,8,4096,128], lengths U{1..4096}:
                           the new K/V row appended at len-1, then decode over len rows, in
                           one launch (attn_decode_append).
@@ -15,6 +17,11 @@ working set (1.07 GB of cache plus 201 MB of prefill inputs) is larger than L2.
 python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 Under torchrun each rank runs the same workload on its own GPU (weak scaling, no
 data-path collective); rank 0 prints one JSON line.
+
+python bench.py --kernel NAME [--batch B] [--iters K] [--warmup W]
+runs one kernel on one workload K times after W warm-up launches and prints its mean
+time per launch (CUDA events) -- the single-kernel mode the ncu summaries under
+profiles/ are taken with.  NAME is one of KERNEL_CASES (see run_kernel_case).
 """
 from __future__ import annotations
 
@@ -52,8 +59,12 @@ def with_nominal(r):
 PREFILL = inputs.CAUSAL_GQA
 DECODE = inputs.BATCHED_DECODE
 FILL_LEN = inputs.CAUSAL_GQA_CACHE_LEN
-WORKLOAD = ("causal GQA prefill B=4 S=2048 H=32 Hk=8 D=128 + cache fill into [4,8,4096,128] + "
+WORKLOAD = ("cache fill into [4,8,4096,128] + causal GQA prefill B=4 S=2048 H=32 Hk=8 D=128 + "
             "batched decode step M=32 H=32 Hk=8 D=128 Lmax=4096 lengths U{1..4096}")
+
+
+KERNEL_CASES = ("prefill", "encoder", "chunked", "fill_pair", "scatter", "decode", "decode_append",
+                "long_decode_step", "rope")
 
 
 def parse_args():
@@ -65,6 +76,10 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-configs", action="store_true", help="skip the per-workload lines")
+    p.add_argument("--kernel", choices=KERNEL_CASES, default=None,
+                   help="single-kernel mode: one workload's kernel, --iters launches (for profilers)")
+    p.add_argument("--batch", type=int, default=None, help="--kernel: sequences (default: the workload's)")
+    p.add_argument("--iters", type=int, default=3, help="--kernel: timed launches")
     return p.parse_args()
 
 
@@ -228,7 +243,7 @@ class Workload:
                                     Dd.Lmax, self.ln, 0.0, self.ws, self.nws)
 
 
-LAUNCHES_PER_STEP = 3   # prefill, cache-fill scatter, decode step (append + decode)
+LAUNCHES_PER_STEP = 3   # cache-fill scatter, prefill, decode step (append + decode)
 
 
 def max_over_ranks(torch, dist, dev, values):
@@ -259,7 +274,7 @@ def run_rkv(args, rank, world, torch, dist):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     W = Workload(torch, rkv, dev)
-    parts = [W.prefill_part, W.fill_part, W.decode_part]
+    parts = [W.fill_part, W.prefill_part, W.decode_part]
 
     def step(evs=None):
         for i, fn in enumerate(parts):
@@ -295,7 +310,7 @@ def run_rkv(args, rank, world, torch, dist):
 
     total_ms, *part_ms = max_over_ranks(torch, dist, dev, [total_ms, *part_ms.tolist()])
     ms_step = total_ms / K
-    prefill_ms, fill_ms, dec_ms = part_ms
+    fill_ms, prefill_ms, dec_ms = part_ms
 
     kv_bytes, dec_all_bytes = decode_bytes(W.lens)
     decode_step_gbs, value = decode_step_value(kv_bytes, 0.0, dec_ms, world)
@@ -542,8 +557,8 @@ def run_e2e(W, torch, rkv, stream, K):
     def step(evs):
         evs[0].record(stream)
         W.q.copy_(hq, non_blocking=True); W.k.copy_(hk, non_blocking=True); W.v.copy_(hv, non_blocking=True)
-        W.prefill_part()
         W.fill_part()
+        W.prefill_part()
         ho.copy_(W.o, non_blocking=True)
         evs[1].record(stream)
         W.dec_in.copy_(hdec, non_blocking=True)       # the decode step's inputs: one copy
@@ -643,8 +658,108 @@ def run_reference(args):
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_kernel_case(args):
+    """One kernel on one workload, --iters launches after --warmup (L2 not flushed in between:
+    under a profiler every launch starts cold anyway).  Workloads:
+      prefill           causal GQA prefill (S=2048, H=32, Hk=8, D=128), --batch sequences (4)
+      encoder           encoder non-causal MHA prefill S=1500 H=8 D=64
+      chunked           the causal GQA sequences' second 1024 tokens behind their first 1024
+                        cached rows (attn_prefill_chunked), --batch sequences (4)
+      fill_pair         the causal GQA prefill with its cache fill fused (attn_prefill_fill_cache)
+      scatter           the causal GQA cache fill (kv_cache_scatter of S rows into [B,8,4096,128])
+      decode            batched decode M=--batch (32) over the seeded lengths (attn_decode_batched)
+      decode_append     the same step with the new rows appended in the launch (attn_decode_append)
+      long_decode_step  the last long-context step: M=1, 32768 rows, append + decode in one launch
+      rope              RoPE prologue of the causal GQA prefill (kv_append_rope, T=2048)"""
+    import dataclasses
+
+    import torch
+    from resident_kv_cache_gb300 import binding as rkv
+    from resident_kv_cache_gb300 import build as rkv_build
+    rkv_build.build()
+    rkv.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    name = args.kernel
+    to = lambda a: torch.from_numpy(a).to(dev)
+    if name in ("prefill", "chunked", "fill_pair", "scatter", "rope"):
+        P = dataclasses.replace(PREFILL, B=args.batch or PREFILL.B)
+        q, k, v = (to(a) for a in inputs.prefill_inputs(P))
+        L = FILL_LEN
+        kc, vc = torch.zeros((P.B, P.Hk, L, P.D), device=dev), torch.zeros((P.B, P.Hk, L, P.D), device=dev)
+        zero = torch.zeros(P.B, dtype=torch.int32, device=dev)
+        if name == "prefill":
+            o = torch.empty_like(q)
+            run = lambda: rkv.attn_prefill(q, k, v, o, P.B, P.S, P.H, P.Hk, P.D, True)
+            work, unit = P.flops / 1e12, "TFLOP/s"
+        elif name == "fill_pair":
+            o = torch.empty_like(q)
+            run = lambda: rkv.attn_prefill_fill_cache(q, k, v, o, P.B, P.S, P.H, P.Hk, P.D, True, kc, vc, L)
+            work, unit = P.flops / 1e12, "TFLOP/s"
+        elif name == "scatter":
+            run = lambda: rkv.kv_cache_scatter(k, v, kc, vc, P.B, P.S, P.Hk, P.D, L, zero)
+            work, unit = scatter_bytes(P.B, P.S, P.Hk, P.D) / 1e9, "GB/s"
+        elif name == "rope":
+            run = lambda: rkv.kv_append_rope(q, k, v, kc, vc, P.B, P.S, P.H, P.Hk, P.D, L, zero, theta=1e4)
+            # q and k rotated in place (read + write), v read, K and V rows written to the cache
+            work, unit = 4.0 * P.B * P.S * (2 * P.H * P.D + 2 * P.Hk * P.D + 3 * P.Hk * P.D) / 1e9, "GB/s"
+        else:
+            c = P.S // 2
+            rkv.kv_cache_scatter(k, v, kc, vc, P.B, P.S, P.Hk, P.D, L, zero)
+            q2 = q[:, c:].contiguous()
+            o2 = torch.empty_like(q2)
+            start = torch.full((P.B,), c, dtype=torch.int32, device=dev)
+            T = P.S - c
+            run = lambda: rkv.attn_prefill_chunked(q2, kc, vc, o2, P.B, T, P.H, P.Hk, P.D, L, True, start)
+            work, unit = 4.0 * P.B * P.H * P.D * (T * c + T * (T + 1) / 2) / 1e12, "TFLOP/s"
+    elif name == "encoder":
+        E = inputs.ENCODER
+        q, k, v = (to(a) for a in inputs.prefill_inputs(E))
+        o = torch.empty_like(q)
+        run = lambda: rkv.attn_prefill(q, k, v, o, E.B, E.S, E.H, E.Hk, E.D, E.causal)
+        work, unit = E.flops / 1e12, "TFLOP/s"
+    elif name in ("decode", "decode_append"):
+        d = dataclasses.replace(DECODE, M=args.batch or DECODE.M)
+        x = inputs.batched_decode_inputs(d)
+        kc, vc, qd, ln = (to(x[n]) for n in ("k_cache", "v_cache", "q", "lens"))
+        kn, vn = to(x["k_new"]), to(x["v_new"])
+        od = torch.empty_like(qd)
+        nws = rkv.attn_decode_workspace_bytes(d.M, d.H, d.Hk, d.D, d.Lmax)
+        ws = torch.zeros(nws, dtype=torch.uint8, device=dev)
+        if name == "decode":
+            run = lambda: rkv.attn_decode_batched(qd, kc, vc, od, d.M, d.H, d.Hk, d.D, d.Lmax, ln, 0.0, ws, nws)
+        else:
+            run = lambda: rkv.attn_decode_append(qd, kn, vn, kc, vc, od, d.M, d.H, d.Hk, d.D, d.Lmax, ln, 0.0,
+                                                 ws, nws)
+        work, unit = (2.0 * d.Hk * d.D * 4 * float(x["lens"].sum()) + 2.0 * d.M * d.H * d.D * 4) / 1e9, "GB/s"
+    else:   # long_decode_step
+        d = inputs.LONG_DECODE
+        t = d.extra["steps"] - 1
+        x = inputs.long_decode_step_inputs(t)
+        kc = to(inputs.normal((1, d.Hk, d.Lmax, d.D), inputs.SEED_K))
+        vc = to(inputs.normal((1, d.Hk, d.Lmax, d.D), inputs.SEED_V))
+        qd, kn, vn = to(x["q"]), to(x["k_new"]), to(x["v_new"])
+        ln = torch.full((1,), x["len"], dtype=torch.int32, device=dev)
+        od = torch.empty_like(qd)
+        nws = rkv.attn_decode_workspace_bytes(1, d.H, d.Hk, d.D, d.Lmax)
+        ws = torch.zeros(nws, dtype=torch.uint8, device=dev)
+        run = lambda: rkv.attn_decode_append(qd, kn, vn, kc, vc, od, 1, d.H, d.Hk, d.D, d.Lmax, ln, 0.0, ws, nws)
+        work, unit = (2.0 * d.Hk * d.D * 4 * x["len"] + 2.0 * d.H * d.D * 4) / 1e9, "GB/s"
+    for _ in range(max(0, args.warmup)):
+        run()
+    torch.cuda.synchronize()
+    ms = time_launches(torch, stream, run, max(1, args.iters))
+    if rkv.rkv_read_device_flags() & rkv.RKV_FLAG_WAIT_TIMEOUT:
+        raise RuntimeError("device reported a wait timeout")
+    print(f"{name}: {ms:.4f} ms per launch, {work / (ms * 1e-3):.1f} {unit}", flush=True)
+
+
 def main():
     args = parse_args()
+    if args.kernel:
+        run_kernel_case(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

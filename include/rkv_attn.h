@@ -95,6 +95,21 @@ rkv_status rkv_read_device_flags(unsigned int* flags, int clear, cudaStream_t st
 rkv_status rkv_check_wait_timeout(unsigned int limit_us, cudaStream_t stream);
 
 /*
+ * Self-check of the operand rounding of the prefill.  The tensor core reads an
+ * f32 operand of a TF32 product by dropping its 13 low mantissa bits; the
+ * prefill first adds half a TF32 unit in the last place to the bit pattern of
+ * each element of Q and V, which makes the drop a round to nearest, ties away
+ * from zero (infinities stay infinite, positive NaNs stay NaN; a negative NaN
+ * at 0xFFFFF000 or above is read as +0).  For each of the n f32 bit patterns in
+ * x this writes ours[i] = that rounding with the low 13 bits cleared, and
+ * ref[i] = the hardware conversion cvt.rna.tf32.f32 of x[i]; the two agree bit
+ * for bit on every finite input.  Device pointers, 4-byte aligned; n >= 0.
+ * Asynchronous on `stream`.  No counterpart on the pages.
+ */
+rkv_status rkv_check_tf32_round(const unsigned int* x, unsigned int* ours, unsigned int* ref, int n,
+                                cudaStream_t stream);
+
+/*
  * Prefill attention over interleaved activations, causal or not, with GQA.
  *
  * Cites: trueno-gpu attention.rs, fn batched_multihead_attention_optimized
@@ -113,7 +128,10 @@ rkv_status rkv_check_wait_timeout(unsigned int limit_us, cudaStream_t stream);
  *   scale    0 -> 1/sqrt(head_dim)
  * Heads are read in place (no head-split copies); no score matrix is stored.
  * Arithmetic: QK^T and PV on TF32 tensor cores with f32 accumulation; softmax
- * in f32.  o must not alias q, k or v.
+ * in f32.  Q and V are rounded to the nearest TF32 value (rkv_check_tf32_round),
+ * K and the probabilities are truncated to TF32 (the probabilities' row sum is
+ * taken over the truncated values).  Non-finite inputs give unspecified rows
+ * (a NaN need not propagate).  o must not alias q, k or v.
  */
 rkv_status attn_prefill(const float* q, const float* k, const float* v, float* o,
                         int batch, int seq_len, int n_heads, int n_kv_heads, int head_dim,

@@ -66,6 +66,8 @@ def load():
     lib.rkv_read_device_flags.argtypes = [ctypes.POINTER(ctypes.c_uint), I, P]
     lib.rkv_check_wait_timeout.restype = I
     lib.rkv_check_wait_timeout.argtypes = [ctypes.c_uint, P]
+    lib.rkv_check_tf32_round.restype = I
+    lib.rkv_check_tf32_round.argtypes = [P, P, P, I, P]
     lib.attn_prefill.restype = I
     lib.attn_prefill.argtypes = [P, P, P, P, I, I, I, I, I, I, P, F, P]
     lib.attn_prefill_fill_cache.restype = I
@@ -137,6 +139,12 @@ def rkv_read_device_flags(clear: bool = False, stream=None) -> int:
 def rkv_check_wait_timeout(limit_us: int, stream=None) -> None:
     """Run the bounded on-chip wait on a barrier nothing completes (gives up after limit_us)."""
     _check("rkv_check_wait_timeout", load().rkv_check_wait_timeout(int(limit_us), _stream(stream)))
+
+
+def rkv_check_tf32_round(x, ours, ref, n, stream=None) -> None:
+    """The prefill's operand rounding (ours) and the hardware cvt.rna.tf32.f32 (ref) of n f32 bit patterns."""
+    _check("rkv_check_tf32_round", load().rkv_check_tf32_round(_ptr(x), _ptr(ours), _ptr(ref), int(n),
+                                                               _stream(stream)))
 
 
 def attn_prefill(q, k, v, o, batch, seq_len, n_heads, n_kv_heads, head_dim, causal,

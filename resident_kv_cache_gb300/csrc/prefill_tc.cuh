@@ -21,8 +21,7 @@
 //   warp 11      V producer (one thread): V tiles into an NV-stage ring, followed per
 //                item by output staging slots that the epilogue fills with O / l and
 //                this thread stores to the output by TMA.
-//   warp 1       QK^T issuer (one thread) and TMEM owner: per item, Q goes from
-//                the K ring into TMEM by tcgen05.cp, then per key block
+//   warp 1       QK^T issuer (one thread) and TMEM owner: per key block
 //                  S_j = Q . K_j^T   tcgen05.mma kind::tf32, A = Q from TMEM
 //                S goes to NSBUF TMEM buffers, so QK^T runs up to NSBUF blocks
 //                ahead of the softmax.
@@ -33,10 +32,15 @@
 //                p = 2^(s*scale*log2e - m) truncated to TF32 and written back over
 //                S; per item: O / l written to the staging slots (swizzled like the
 //                TMA box, conflict-free).
-//   warps 6-9    V transposer: tcgen05 kind::tf32 reads B only K-major, so each
-//                V tile is transposed in shared memory (4x4 blocks through
-//                registers, conflict-free 16-byte loads and stores, 128-byte swizzle).
-// Q, K and V stay f32; the tensor core reads them as TF32 by truncation.
+//   warps 6-9    Q and V^T: per item, the query tile goes from the K ring through
+//                registers (rounded to nearest TF32) into TMEM by tcgen05.st; tcgen05
+//                kind::tf32 reads B only K-major, so each V tile is transposed in
+//                shared memory (4x4 blocks through registers, rounded to nearest TF32,
+//                conflict-free 16-byte loads and stores, 128-byte swizzle).
+// Q, K and V stay f32 in memory.  The tensor core reads an f32 operand as TF32 by dropping
+// its low 13 bits: K is used as loaded (truncated), Q and V are rounded to nearest on their
+// way through registers (half the worst-case error of truncation, no bias), P is truncated
+// and the row sum is taken over exactly the truncated values.
 // Every mbarrier wait is time-bounded (see rkv_internal.cuh); a CTA that gives
 // up unwinds: it drains its own copies in flight, lets issued MMAs finish and
 // frees its TMEM.
@@ -99,8 +103,8 @@ struct PfCfg {
     static constexpr int OFF_V = OFF_K + NK * TILE;
     static constexpr int OFF_BAR = OFF_V + NV * TILE;
     // barriers: k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], v_loaded[NV], s_full[NSBUF],
-    //           p_ready[NSBUF], o_done[NSBUF], o_final, q_free, o_free, drain, drain_pv
-    static constexpr int NBAR = 2 * NK + 3 * NV + 3 * NSBUF + 5;
+    //           p_ready[NSBUF], o_done[NSBUF], o_final, q_free, o_free, drain, drain_pv, q_ready
+    static constexpr int NBAR = 2 * NK + 3 * NV + 3 * NSBUF + 6;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;     // tmem base, abort flag
     static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM = (SMEM_USED + 1024 > kPfMinSmem ? SMEM_USED + 1024 : kPfMinSmem);
@@ -111,7 +115,7 @@ struct PfCfg {
 
 struct PfBars {
     uint32_t k_full, k_empty, v_full, v_empty, v_loaded, s_full, p_ready, o_done, o_final, q_free, o_free,
-        drain, drain_pv;
+        drain, drain_pv, q_ready;
 };
 
 template <int NK, int NV, int NSB>
@@ -130,6 +134,7 @@ __device__ __forceinline__ PfBars pf_bars(uint32_t base) {
     b.o_free = b.q_free + 8;
     b.drain = b.o_free + 8;
     b.drain_pv = b.drain + 8;
+    b.q_ready = b.drain_pv + 8;
     return b;
 }
 
@@ -181,9 +186,12 @@ __device__ __forceinline__ int pf_item(int k) {
 // engine and clipped on store) and the kernel carries none of that code.
 // FILL: the launch is followed by a programmatic dependent (the cache fill, kv_scatter.cu),
 // which this kernel releases at once so that it runs beside the attention, in the registers and
-// shared memory the prefill leaves free on each SM.
+// shared memory the prefill leaves free on each SM.  For that the FILL variant at D = 128 is
+// held to kPfFillRegs registers a thread: 384 x 144 + the fill's 256 x 40 fill the 64K
+// register file (at D <= 64 the kernel needs more, and the fill runs in what is left).
+constexpr int kPfFillRegs = 144;
 template <int D, bool GUARD, bool FILL>
-__global__ void __launch_bounds__(kPfThreads, 1)
+__global__ void __maxnreg__(FILL && D == 128 ? kPfFillRegs : 65536 / kPfThreads / 8 * 8)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
                   float* __restrict__ o,
@@ -238,6 +246,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         mbar_init(bar.o_free, 128);
         mbar_init(bar.drain, 1);
         mbar_init(bar.drain_pv, 1);
+        mbar_init(bar.q_ready, 128);
         *abort_flag = 0;
         fence_barrier_init();
         prefetch_tmap(&tm_k);
@@ -400,26 +409,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                         mbar_arrive(bar.k_empty + 8 * (f % C::NK));
                         ++f;
                     }
-                    // Q -> TMEM columns kColQ.. by tcgen05.cp, once the previous item's QK^T
-                    // MMAs (committed to q_free) are done reading them.  The copies run ahead
-                    // of this thread's later MMAs in issue order.
-                    if (t > 0) ok = mbar_wait(bar.q_free, (uint32_t)(t - 1) & 1u, abort_flag, flags);
-                    for (int i = 0; ok && i < C::QSLOTS; ++i)
-                        ok = mbar_wait(bar.k_full + 8 * ((f + i) % C::NK), (uint32_t)((f + i) / C::NK) & 1u, abort_flag,
-                                       flags);
-                    if (!ok) break;
+                    // The Q/V^T warps read the item's query tile out of the K ring, round it and
+                    // write it into TMEM columns kColQ.. (after the previous item's QK^T MMAs,
+                    // committed to q_free, are done reading them).  Once they have, the query
+                    // slots are handed back to the K producer.
+                    if (!(ok = mbar_wait(bar.q_ready, (uint32_t)t & 1u, abort_flag, flags))) break;
                     tc_fence_after();
-                    {
-                        const int sq = f % C::NK;    // even when paired: the query tile fills a slot pair
-#pragma unroll
-                        for (int kk8 = 0; kk8 < D / 8; ++kk8) {
-                            const int c = kk8 / (C::CH / 8), kk = kk8 % (C::CH / 8);
-                            tmem_cp_128x256b(tmem + kColQ + 8 * kk8,
-                                             kdesc0 + (uint64_t)((C::koff(sq, c) + kk * 32) >> 4));
-                        }
-                        for (int i = 0; i < C::QSLOTS; ++i) mma_commit(bar.k_empty + 8 * ((f + i) % C::NK));
-                        f += C::QSLOTS;
-                    }
+                    for (int i = 0; i < C::QSLOTS; ++i) mbar_arrive(bar.k_empty + 8 * ((f + i) % C::NK));
+                    f += C::QSLOTS;
                     // S of block gb goes to buffer gb % NSBUF.  Paired blocks (D = 128: fill f
                     // even, adjacent buffers) share one N = 2*BN chain.  Before QK overwrites a
                     // buffer, the PV that read P from it (block gb - NSBUF) must have finished.
@@ -498,7 +495,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             }
         }
     } else if (warp >= kPfVWarp0 && warp < kPfVWarp0 + 4) {
-        // ================================================================ V transposer
+        // ================================================================ Q and V^T
+        // Per item, first the query tile: each thread takes its query row (TMEM lane) out of
+        // the K ring (swizzled rows: 16-byte chunk j of row r at j ^ (r & 7), or j ^ ((r >> 1)
+        // & 3) with the 64-byte swizzle; conflict-free, eight consecutive rows per quarter-warp),
+        // rounds it to nearest TF32 and stores it into TMEM columns kColQ.. of its lane.
         // V tiles arrive by TMA in the same swizzled layout as K (rows = keys).  The
         // transposer rewrites each slot in place as V^T: work item = (key quad aa,
         // d quad dq), a 4x4 block read with four 16-byte loads and written as four
@@ -513,7 +514,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         constexpr int LDQ = D / 4 < 8 ? D / 4 : 8;           // D = 16: lanes along d quads
         constexpr int LAA = 32 / LDQ;                        // D = 16: lanes along key quads
         constexpr int GA = (BN / 4) / LAA;                   // D = 16: lane groups along keys
-        constexpr int GD = (D / 4) / LDQ;                    // D = 16: lane groups along d
         constexpr int PER = (BN / 4) * (D / 4) / 128;        // 4x4 blocks per thread per tile
         static_assert((BN / 4) * (D / 4) % 128 == 0 && PER >= 1, "V transposer work split");
         static_assert(D < 32 || (BN % 32 == 0 && D % 32 == 0), "diagonal transposer map");
@@ -542,11 +542,60 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         };
         bool ok = true;
         int gb = 0;                                          // V-ring fills passed
+        int fk = 0;                                          // K-ring fills passed (as the QK^T issuer)
+        int tq = 0;                                          // items with keys so far
+        const int qquad = warp & 3;                          // TMEM lane quadrant of this warp
+        const int qr = qquad * 32 + lane;                    // query row within the tile
         for (int k = 0; ok; ++k) {
             const int u = pf_item(k);
             if (u >= n_work) break;
             const PfWork w = work(u);
             if (w.nblk == 0) continue;
+            // ---- query tile of this item -> TMEM (the previous item's QK^T done with it)
+            if (C::KPAIR && (fk & 1)) ++fk;                  // pad fill
+            {
+                bool okq = true;
+                if (tq > 0) okq = mbar_wait(bar.q_free, (uint32_t)(tq - 1) & 1u, abort_flag, flags);
+                for (int i = 0; okq && i < C::QSLOTS; ++i)
+                    okq = mbar_wait(bar.k_full + 8 * ((fk + i) % C::NK), (uint32_t)((fk + i) / C::NK) & 1u,
+                                    abort_flag, flags);
+                if (!(ok = __all_sync(0xffffffffu, okq))) break;   // warp-uniform before TMEM access
+                tc_fence_after();
+                const uint32_t qlane = tmem + ((uint32_t)(qquad * 32) << 16);
+                const int sq = fk % C::NK;      // even when paired: the query tile fills a slot pair
+#pragma unroll 1
+                for (int c = 0; c < C::NCH; ++c) {
+                    const unsigned char* row = smem + C::OFF_K + C::koff(sq, c) + qr * (C::CH * 4);
+                    if constexpr (C::CH == 32) {
+                        uint32_t wv[32];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const uint4 x = *reinterpret_cast<const uint4*>(row + ((j ^ (qr & 7)) << 4));
+                            wv[4 * j] = tf32_round_bits(x.x);
+                            wv[4 * j + 1] = tf32_round_bits(x.y);
+                            wv[4 * j + 2] = tf32_round_bits(x.z);
+                            wv[4 * j + 3] = tf32_round_bits(x.w);
+                        }
+                        tmem_st32(qlane + kColQ + 32 * c, wv);
+                    } else {                    // D = 16: 64-byte rows, 64-byte swizzle
+                        uint32_t wv[16];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint4 x = *reinterpret_cast<const uint4*>(row + ((j ^ ((qr >> 1) & 3)) << 4));
+                            wv[4 * j] = tf32_round_bits(x.x);
+                            wv[4 * j + 1] = tf32_round_bits(x.y);
+                            wv[4 * j + 2] = tf32_round_bits(x.z);
+                            wv[4 * j + 3] = tf32_round_bits(x.w);
+                        }
+                        tmem_st16(qlane + kColQ, wv);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar.q_ready);
+                fk += C::QSLOTS + w.nblk;
+                ++tq;
+            }
             // ---- V tiles of this item
             for (int j = 0; j < w.nblk; ++j, ++gb) {
                 const int s = gb % C::NV;
@@ -582,11 +631,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     blk(it, aa, dq);
                     const int kc = aa >> 3;                      // 32-key chunk of the V^T row
                     const float4 c0 = x[it][0], c1 = x[it][1], c2 = x[it][2], c3 = x[it][3];
-                    const uint4 wr[4] = {
-                        make_uint4(__float_as_uint(c0.x), __float_as_uint(c1.x), __float_as_uint(c2.x), __float_as_uint(c3.x)),
-                        make_uint4(__float_as_uint(c0.y), __float_as_uint(c1.y), __float_as_uint(c2.y), __float_as_uint(c3.y)),
-                        make_uint4(__float_as_uint(c0.z), __float_as_uint(c1.z), __float_as_uint(c2.z), __float_as_uint(c3.z)),
-                        make_uint4(__float_as_uint(c0.w), __float_as_uint(c1.w), __float_as_uint(c2.w), __float_as_uint(c3.w))};
+                    auto rb = [](float x) { return tf32_round_bits(__float_as_uint(x)); };
+                    const uint4 wr[4] = {make_uint4(rb(c0.x), rb(c1.x), rb(c2.x), rb(c3.x)),
+                                         make_uint4(rb(c0.y), rb(c1.y), rb(c2.y), rb(c3.y)),
+                                         make_uint4(rb(c0.z), rb(c1.z), rb(c2.z), rb(c3.z)),
+                                         make_uint4(rb(c0.w), rb(c1.w), rb(c2.w), rb(c3.w))};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int d = dq * 4 + i;

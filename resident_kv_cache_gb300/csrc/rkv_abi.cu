@@ -160,6 +160,33 @@ rkv_status rkv_check_wait_timeout(unsigned int limit_us, cudaStream_t stream) {
     return check_launch("rkv_check_wait_timeout");
 }
 
+// Each element: ours = the prefill's operand rounding with the 13 bits the tensor core drops
+// cleared; ref = the hardware conversion to TF32 with round-to-nearest, ties away.
+__global__ void tf32_round_check_kernel(const uint32_t* __restrict__ x, uint32_t* __restrict__ ours,
+                                        uint32_t* __restrict__ ref, int n) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const uint32_t b = x[i];
+        ours[i] = tf32_round_bits(b) & 0xFFFFE000u;
+        uint32_t r;
+        asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(__uint_as_float(b)));
+        ref[i] = r;
+    }
+}
+
+rkv_status rkv_check_tf32_round(const unsigned int* x, unsigned int* ours, unsigned int* ref, int n,
+                                cudaStream_t stream) {
+    const char* op = "rkv_check_tf32_round";
+    g_msg[0] = 0;
+    if (n < 0) return set_error(RKV_ERR_INVALID_ARG, "%s: n must be >= 0, got %d", op, n);
+    if (n == 0) return RKV_OK;
+    if (!x || !ours || !ref) return set_error(RKV_ERR_INVALID_ARG, "%s: x, ours and ref must be non-NULL", op);
+    if (!aligned(x, 4) || !aligned(ours, 4) || !aligned(ref, 4))
+        return set_error(RKV_ERR_INVALID_ARG, "%s: x, ours and ref must be 4-byte aligned", op);
+    const int blocks = (int)(((int64_t)n + 255) / 256 < 4096 ? ((int64_t)n + 255) / 256 : 4096);
+    tf32_round_check_kernel<<<blocks, 256, 0, stream>>>(x, ours, ref, n);
+    return check_launch(op);
+}
+
 rkv_status attn_prefill(const float* q, const float* k, const float* v, float* o, int batch, int seq_len,
                         int n_heads, int n_kv_heads, int head_dim, int causal, const int* seq_lens,
                         float scale, cudaStream_t stream) {

@@ -246,14 +246,6 @@ __device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 }
 
 // Arrive on an mbarrier once every tcgen05 op issued so far by this thread completes.
-// Copy a 128-row x 256-bit slice (8 columns of 32 bits) from shared memory, described
-// like an MMA operand, into TMEM lanes 0..127 at columns taddr..taddr+7.  Asynchronous;
-// runs in issue order ahead of later tcgen05.mma of the same thread and is tracked by
-// tcgen05.commit.
-__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -284,6 +276,20 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
     uint64_t r;
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
+}
+
+// An f32 operand of a kind::tf32 MMA is read as TF32 by dropping its 13 low mantissa bits.
+// Adding half a TF32 unit in the last place (2^12 in the bit pattern) first turns that drop
+// into rounding to nearest, ties away from zero (IEEE 754 roundTiesToAway at 10 fraction bits):
+// the carry reaches bit 13 exactly when the dropped part is at least half a unit.  For a
+// negative number the bit pattern read as a signed integer grows with the magnitude too, so
+// one add serves both signs.  The add and a signed max with the input are one instruction
+// (VIADDMNMX): a positive NaN whose top fraction bits are all set (the canonical 0x7FFFFFFF
+// among them) would carry into the sign bit and is kept as it is instead.  Infinities stay
+// infinite; a negative NaN at 0xFFFFF000 or above wraps to a tiny positive number and is read
+// as +0.  The low 13 bits of the result are left for the tensor core to drop.
+__device__ __forceinline__ uint32_t tf32_round_bits(uint32_t b) {
+    return (uint32_t)__viaddmax_s32((int)b, 0x1000, (int)b);
 }
 
 __device__ __forceinline__ void tmem_wait_ld() {

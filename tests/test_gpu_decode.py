@@ -104,6 +104,7 @@ def test_one_workspace_serves_calls_of_different_sizes(rkv, oracle_mod):
     tickets never land on a smaller call's records.  Lengths are long enough that every
     (sequence, kv head) is split over several CTAs and merged through its ticket."""
     torch = torch_cuda()
+    rkv.rkv_read_device_flags(clear=True)   # flags left by earlier tests
     H, D, L = 32, 128, 4096
     shapes = [(8, 8), (16, 8), (8, 8), (4, 16), (16, 8), (2, 32)]   # (M, Hk)
     n = max(rkv.attn_decode_workspace_bytes(M, H, Hk, D, L) for M, Hk in shapes)

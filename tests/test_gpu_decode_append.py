@@ -81,3 +81,58 @@ def test_decode_append_batched_decode_workload(rkv):
     torch.cuda.synchronize()
     assert torch.equal(o1, o2)
     assert torch.equal(k1, k2) and torch.equal(v1, v2)
+
+
+def test_long_context_decode_as_timed(rkv, oracle_mod):
+    """The long-context decode exactly as it is timed: M=1, H=32, Hk=8, D=128, cache
+    [1,8,32768,128] prefilled to 32512 rows, 256 steps of attn_decode_append (row 32512+t
+    appended and 32513+t rows attended; one (sequence, kv head) split over every CTA and
+    merged in the launch), issued eagerly and replayed from one CUDA graph.  Steps 0, 1, 127
+    and 255 are checked against the oracle (trueno-gpu fn kv_cache_scatter_gpu then
+    fn incremental_attention_gpu), the graph replay against the eager run bit for bit, and
+    the final caches against the oracle's scatter bit for bit."""
+    torch = torch_cuda()
+    rkv.rkv_read_device_flags(clear=True)   # flags left by earlier tests
+    d = inputs.LONG_DECODE
+    H, Hk, D, L, T = d.H, d.Hk, d.D, d.Lmax, d.extra["steps"]
+    k0 = inputs.normal((1, Hk, L, D), inputs.SEED_K)
+    v0 = inputs.normal((1, Hk, L, D), inputs.SEED_V)
+    steps = [inputs.long_decode_step_inputs(t) for t in range(T)]
+    qs = torch.from_numpy(np.stack([x["q"] for x in steps])).cuda()
+    kn = torch.from_numpy(np.stack([x["k_new"] for x in steps])).cuda()
+    vn = torch.from_numpy(np.stack([x["v_new"] for x in steps])).cuda()
+    lens = torch.tensor([x["len"] for x in steps], dtype=torch.int32, device="cuda")
+    n = rkv.attn_decode_workspace_bytes(1, H, Hk, D, L)
+
+    def run(kc, vc, ws, outs):
+        for t in range(T):
+            rkv.attn_decode_append(qs[t], kn[t], vn[t], kc, vc, outs[t], 1, H, Hk, D, L, lens[t:t + 1], 0.0,
+                                   ws, n)
+
+    ka, va = torch.from_numpy(k0).cuda(), torch.from_numpy(v0).cuda()
+    wa = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    oa = torch.full((T, 1, H * D), float("nan"), device="cuda")
+    run(ka, va, wa, oa)
+    torch.cuda.synchronize()
+    kb, vb = torch.from_numpy(k0).cuda(), torch.from_numpy(v0).cuda()
+    wb = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    ob = torch.full((T, 1, H * D), float("nan"), device="cuda")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run(kb, vb, wb, ob)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(ob, oa), "graph replay differs from the eager launches"
+    assert torch.equal(kb, ka) and torch.equal(vb, va)
+    assert rkv.rkv_read_device_flags(clear=True) == 0
+
+    got = oa.cpu().numpy()
+    kn_all = np.concatenate([x["k_new"] for x in steps], axis=1)   # [1, 256, Hk*D]
+    vn_all = np.concatenate([x["v_new"] for x in steps], axis=1)
+    start = np.array([inputs.LONG_DECODE_PREFILLED], np.int32)
+    for t in (0, 1, 127, 255):
+        hk, hv, _ = oracle_mod.scatter(kn_all[:, :t + 1], vn_all[:, :t + 1], k0, v0, 1, t + 1, Hk, D, L, start)
+        want = oracle_mod.decode(steps[t]["q"], hk, hv, 1, H, Hk, D, L, np.array([steps[t]["len"]]))
+        assert_close(got[t], want, 1e-4, what=f"step {t}")
+    hk, hv, _ = oracle_mod.scatter(kn_all, vn_all, k0, v0, 1, T, Hk, D, L, start)
+    assert np.array_equal(ka.cpu().numpy(), hk) and np.array_equal(va.cpu().numpy(), hv)

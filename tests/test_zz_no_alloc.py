@@ -35,6 +35,7 @@ def test_noalloc_matches_workspace_entry_point_twice(rkv, oracle_mod, M, H, Hk, 
     """Same kernel, same arithmetic, same split of the rows: the output must equal
     attn_decode_batched's bit for bit, on both calls, and match the oracle."""
     torch = torch_cuda()
+    rkv.rkv_read_device_flags(clear=True)   # flags left by earlier tests
     if lens is None:
         lens = inputs.uniform_lengths(M, 1, L, inputs.SEED_LEN)
     q, kc, vc, ln = _inputs(torch, M, H, Hk, D, L, lens, seed=M + D)
