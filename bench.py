@@ -159,7 +159,8 @@ def kernel_hash(*files):
     return h.hexdigest()[:16]
 
 
-KERNEL_FILES = {"prefill": ("prefill_tc.cuh", "prefill_tc.cu"), "decode": ("decode_splitkv.cu",), "scatter": ("kv_scatter.cu",)}
+KERNEL_FILES = {"prefill": ("prefill_tc.cuh", "prefill_tc.cu", "rkv_internal.cuh"),
+                "decode": ("decode_splitkv.cu", "rkv_internal.cuh"), "scatter": ("kv_scatter.cu",)}
 
 
 def ncu_traffic(kernel):

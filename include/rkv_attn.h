@@ -283,10 +283,11 @@ rkv_status attn_decode_batched_noalloc(const float* q, const float* k_cache,
  *   k_cache, v_cache                        updated in place at row seq_lens[m]-1
  *                                           (not written when that row is
  *                                           outside [0, max_len))
- * Every other argument as attn_decode_batched.  The row of a (sequence, kv
- * head) is written by the one CTA that also reads it, before its bulk copies
- * start, so no separate launch or grid-wide ordering is needed.  Outputs must
- * not alias the inputs.
+ * Every other argument as attn_decode_batched.  The new row is the last row
+ * each (sequence, kv head) attends to; the one CTA that reads it takes it
+ * straight from k_new / v_new and writes it into the cache when it is done
+ * with its rows, so no separate launch, grid-wide ordering or wait on the
+ * write is needed.  Outputs must not alias the inputs.
  */
 rkv_status attn_decode_append(const float* q, const float* k_new, const float* v_new,
                               float* k_cache, float* v_cache, float* o, int M, int n_heads,

@@ -26,9 +26,11 @@
 //    workspace, and the last CTA to finish a segment (atomic ticket) merges the
 //    records with the log-sum-exp rule, one warp per query head, and resets the
 //    ticket to zero.
-//  * With k_new / v_new (the one-launch decode step), the CTA whose share holds
-//    row len-1 of a segment first writes the new row there, then fences it
-//    before its own bulk copies read it.
+//  * With k_new / v_new (the one-launch decode step), the new row of a segment is its
+//    last row, len-1.  The CTA whose share holds it copies that row into its last tile
+//    straight from k_new / v_new (the tile's other rows come from the cache), so no
+//    copy of this launch reads cache row len-1, and the consumer warps write the new
+//    rows into the cache after their last piece, with nothing waiting on the stores.
 #include "rkv_internal.cuh"
 #include "rkv_launch.h"
 
@@ -64,7 +66,7 @@ struct DecCfg {
     // shared memory layout (bytes): as many K/V stages as fit beside the reduction buffers
     static constexpr int TILE_BYTES = TILE_ROWS * D * 4;
     static constexpr int SIDE = W * ENTRIES * 4 + W * G * D * 4 + W * 2 * G * 4 + 34 * 8 + 32 * 4 + 2 * 4 * 8 + 16 +
-                                2 * 32 * 8;
+                                2 * 32 * 8 + 32 * 4;
     static constexpr int NST_FIT = (226 * 1024 - SIDE) / (2 * TILE_BYTES);
     static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;          // pipeline stages
     static_assert(NST >= 2, "decode pipeline needs two stages");
@@ -77,7 +79,8 @@ struct DecCfg {
     static constexpr int OFF_BAR = OFF_L + 32 * 4;                                // full/empty
     static constexpr int OFF_MISC = OFF_BAR + 2 * NST * 8;                        // abort, last
     static constexpr int OFF_PTR = OFF_MISC + 16;                                 // per-sequence K, V bases
-    static constexpr int SMEM = OFF_PTR + 2 * 32 * 8;
+    static constexpr int OFF_APP = OFF_PTR + 2 * 32 * 8;                          // int APP[32]
+    static constexpr int SMEM = OFF_APP + 32 * 4;
     static_assert(SMEM <= 227 * 1024, "decode shared memory budget");
     static_assert(NV >= 1 && (LPR & (LPR - 1)) == 0, "lane split");
 };
@@ -148,6 +151,7 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC);
     volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    int* APP = reinterpret_cast<int*>(smem + C::OFF_APP);   // [m]: a new row goes to row L[m]-1
     const float** kbase = reinterpret_cast<const float**>(smem + C::OFF_PTR);   // [32]
     const float** vbase = kbase + 32;
 
@@ -175,6 +179,9 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
             kbase[lane] = kb;
             vbase[lane] = vb;
             L[lane] = len;
+            // the step's new row lands at len-1 only for a length in [1, max_len] (unclamped) and a
+            // usable cache; it is then the last row of each of the sequence's segments
+            APP[lane] = k_new != nullptr && len > 0 && len == __ldg(seq_lens + lane);
         }
         int64_t rows = (int64_t)len * Hk, incl = rows;
 #pragma unroll
@@ -196,30 +203,6 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
 
     const int64_t R = P[M];
     const int64_t r0 = share_begin(c, R, n), r1 = share_begin(c + 1, R, n);
-
-    if (k_new) {
-        // Fused append: the new K/V row of each (sequence, kv head) goes to cache row len-1 first.
-        // That row is read by exactly one CTA -- the one whose share holds it -- so that CTA writes
-        // it here, and a proxy fence orders the stores before its own bulk copies read the row.
-        // (A row past max_len is not written, as kv_cache_scatter skips it.)
-        for (int sg = warp; sg < M * Hk && warp < C::W; sg += C::W) {
-            const int m = sg / Hk, kh = sg - m * Hk;
-            const int p = __ldg(seq_lens + m) - 1;        // append position, from the unclamped length
-            if (p < 0 || p >= Lmax || L[m] == 0) continue;
-            const int64_t flat = P[m] + (int64_t)kh * L[m] + p;
-            if (flat < r0 || flat >= r1) continue;
-            const float4* kn = reinterpret_cast<const float4*>(k_new + ((int64_t)m * Hk + kh) * D);
-            const float4* vn = reinterpret_cast<const float4*>(v_new + ((int64_t)m * Hk + kh) * D);
-            float4* kd = reinterpret_cast<float4*>(const_cast<float*>(kbase[m]) + ((int64_t)kh * Lmax + p) * D);
-            float4* vd = reinterpret_cast<float4*>(const_cast<float*>(vbase[m]) + ((int64_t)kh * Lmax + p) * D);
-            for (int i = lane; i < D / 4; i += 32) {
-                kd[i] = __ldg(kn + i);
-                vd[i] = __ldg(vn + i);
-            }
-        }
-        fence_proxy_async_global();
-        __syncthreads();
-    }
 
     if (warp == C::W) {
         // ================================================================ producer
@@ -245,14 +228,24 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
                     const uint32_t ph = (uint32_t)(it / C::NST) & 1u;
                     if (!mbar_wait(smem_addr(&bars[C::NST + s]), ph ^ 1u, abort_flag, flags)) { ok = false; break; }
                     const int rows = (int)min((int64_t)C::TILE_ROWS, piece_end - t0);
-                    const uint32_t bytes = (uint32_t)rows * D * 4;
+                    // the tile that ends a segment with a new row takes that row from k_new / v_new
+                    const bool new_row = APP[m] && t0 + rows == seg_start + L[m];
+                    const int cache_rows = rows - (new_row ? 1 : 0);
+                    const uint32_t bytes = (uint32_t)cache_rows * D * 4;
                     const uint32_t full = smem_addr(&bars[s]);
-                    mbar_arrive_expect_tx(full, 2 * bytes);
+                    const uint32_t k_dst = smem_addr(smem + C::OFF_STAGES + (2 * s) * C::TILE_BYTES);
+                    const uint32_t v_dst = smem_addr(smem + C::OFF_STAGES + (2 * s + 1) * C::TILE_BYTES);
+                    mbar_arrive_expect_tx(full, 2u * (uint32_t)rows * D * 4);
                     const int64_t src = (head_row0 + t0) * D;
-                    bulk_g2s_hint(smem_addr(smem + C::OFF_STAGES + (2 * s) * C::TILE_BYTES), kb + src, bytes, full,
-                                  stream_policy);
-                    bulk_g2s_hint(smem_addr(smem + C::OFF_STAGES + (2 * s + 1) * C::TILE_BYTES), vb + src, bytes,
-                                  full, stream_policy);
+                    if (cache_rows > 0) {
+                        bulk_g2s_hint(k_dst, kb + src, bytes, full, stream_policy);
+                        bulk_g2s_hint(v_dst, vb + src, bytes, full, stream_policy);
+                    }
+                    if (new_row) {
+                        const int64_t nr = ((int64_t)m * Hk + kh) * D;
+                        bulk_g2s_hint(k_dst + bytes, k_new + nr, D * 4, full, stream_policy);
+                        bulk_g2s_hint(v_dst + bytes, v_new + nr, D * 4, full, stream_policy);
+                    }
                     issued[s] = it + 1;
                 }
                 pos = piece_end;
@@ -569,6 +562,25 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
         }
         named_barrier(1, C::CT);   // red_* free for the next piece
         pos = piece_end;
+    }
+    if (k_new) {
+        // The step's new rows into the cache, for the segments whose last row is in this CTA's
+        // share.  No copy of this launch reads those rows (their tiles took them from k_new /
+        // v_new), so the stores wait for nothing and nothing waits for them.
+        for (int sg = warp; sg < M * Hk; sg += C::W) {
+            const int m = sg / Hk, kh = sg - m * Hk;
+            if (!APP[m]) continue;
+            const int64_t flat = P[m] + (int64_t)(kh + 1) * L[m] - 1;
+            if (flat < r0 || flat >= r1) continue;
+            const int64_t row = ((int64_t)kh * Lmax + L[m] - 1) * D;
+            const int64_t nr = ((int64_t)m * Hk + kh) * D;
+            for (int i = lane; i < D / 4; i += 32) {
+                reinterpret_cast<float4*>(const_cast<float*>(kbase[m]) + row)[i] =
+                    __ldg(reinterpret_cast<const float4*>(k_new + nr) + i);
+                reinterpret_cast<float4*>(const_cast<float*>(vbase[m]) + row)[i] =
+                    __ldg(reinterpret_cast<const float4*>(v_new + nr) + i);
+            }
+        }
     }
 }
 
