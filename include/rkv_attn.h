@@ -58,6 +58,9 @@ typedef enum {
 #define RKV_FLAG_NEGATIVE_INPUT  0x4u  /* a negative length or position was treated as 0 / skipped */
 #define RKV_FLAG_BAD_POINTER     0x8u  /* a per-sequence cache pointer was NULL or not 16-byte aligned: that
                                           sequence was skipped (no row read or written, zero output) */
+#define RKV_FLAG_BOUNDS          0x10u /* checked build only (librkv_attn_checked.so, device checks compiled
+                                          in): an index a kernel computed fell outside its buffer and that
+                                          access was skipped -- a defect in the library, never expected */
 
 /* Bytes at the head of a decode workspace that hold its completion tickets
  * (attn_decode_batched and the other decode entry points).  Their place does

@@ -20,6 +20,7 @@ HEADER = os.path.join(_build.INCLUDE, "rkv_attn.h")
 
 RKV_OK, RKV_ERR_INVALID_ARG, RKV_ERR_UNSUPPORTED, RKV_ERR_LAUNCH, RKV_ERR_DEVICE = range(5)
 RKV_FLAG_WAIT_TIMEOUT, RKV_FLAG_LEN_CLAMPED, RKV_FLAG_NEGATIVE_INPUT, RKV_FLAG_BAD_POINTER = 0x1, 0x2, 0x4, 0x8
+RKV_FLAG_BOUNDS = 0x10   # raised only by the checked build
 RKV_DECODE_TICKET_BYTES = 32768   # head of a decode workspace: completion tickets
 
 _lib = None

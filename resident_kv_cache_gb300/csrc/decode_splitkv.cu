@@ -235,6 +235,14 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
                     const uint32_t full = smem_addr(&bars[s]);
                     const uint32_t k_dst = smem_addr(smem + C::OFF_STAGES + (2 * s) * C::TILE_BYTES);
                     const uint32_t v_dst = smem_addr(smem + C::OFF_STAGES + (2 * s + 1) * C::TILE_BYTES);
+                    // (checked build) rows of this sequence's cache, and its row of k_new / v_new
+                    if (!in_bounds(head_row0 + t0, (int64_t)Hk * Lmax, flags) ||
+                        !in_bounds(head_row0 + t0 + rows - 1, (int64_t)Hk * Lmax, flags) ||
+                        !in_bounds((int64_t)m * Hk + kh, (int64_t)M * Hk, flags)) {
+                        mbar_arrive(full);        // no copy: the consumers see stale rows, the flag says so
+                        issued[s] = it + 1;
+                        continue;
+                    }
                     mbar_arrive_expect_tx(full, 2u * (uint32_t)rows * D * 4);
                     const int64_t src = (head_row0 + t0) * D;
                     if (cache_rows > 0) {
@@ -265,7 +273,8 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
         const int m = sg / Hk, kh = sg % Hk;
         if (L[m] == 0)
             for (int i = threadIdx.x; i < G * D; i += C::CT)
-                out[(int64_t)m * H * D + (int64_t)(kh * G) * D + i] = 0.0f;
+                if (in_bounds((int64_t)m * H * D + (int64_t)(kh * G) * D + i, (int64_t)M * H * D, flags))
+                    out[(int64_t)m * H * D + (int64_t)(kh * G) * D + i] = 0.0f;
     }
 
     const int seg = lane % C::LPR;         // float4 column of this lane
@@ -285,12 +294,14 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
         const int64_t seg_end = seg_start + L[m];
         const int64_t piece_end = min(r1, seg_end);
         // q of the G heads sharing kv head kh, pre-scaled so scores are in log2 units
+        const bool q_ok = in_bounds((int64_t)m * H * D + (int64_t)(kh * G + G) * D - 1, (int64_t)M * H * D, flags);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
 #pragma unroll
             for (int f = 0; f < C::FPL; ++f) {
-                float4 t = __ldg(reinterpret_cast<const float4*>(q + (int64_t)m * H * D + (int64_t)(kh * G + h) * D) +
-                                 seg + f * C::LPR);
+                float4 t = q_ok ? __ldg(reinterpret_cast<const float4*>(q + (int64_t)m * H * D + (int64_t)(kh * G + h) * D) +
+                                        seg + f * C::LPR)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
                 qv[h][f] = make_float4(t.x * scale_log2, t.y * scale_log2, t.z * scale_log2, t.w * scale_log2);
             }
 #pragma unroll
@@ -476,6 +487,10 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
         const bool single = (c_first == c_last);
         float* my_rec = records + (int64_t)(sg + c) * C::REC;
         float* o_seg = out + (int64_t)m * H * D + (int64_t)(kh * G) * D;
+        // (checked build) this piece's record, its segment's ticket and output rows
+        const bool io_ok = in_bounds((int64_t)sg + c, (int64_t)M * Hk + kDecMaxCtas, flags) &&
+                           in_bounds(sg, kDecodeTicketSlots, flags) &&
+                           in_bounds((int64_t)m * H * D + (int64_t)(kh * G) * D + G * D - 1, (int64_t)M * H * D, flags);
         for (int i = threadIdx.x; i < G * D; i += C::CT) {
             const int h = i / D, d = i % D;
             float mx = -INFINITY;
@@ -491,7 +506,9 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
                     o += red_acc[(w * G + h) * D + d] * f;
                 }
             }
-            if (single) {
+            if (!io_ok) {
+                // skipped
+            } else if (single) {
                 o_seg[i] = l > 0.0f ? o / l : 0.0f;
             } else {
                 my_rec[i] = o;
@@ -513,7 +530,7 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
                         pieces += share_begin(cc, R, n) < share_begin(cc + 1, R, n);
                 }
                 int last = 0;
-                if (ok) last = (atomicAdd(tickets + sg, 1) == pieces - 1);
+                if (ok && io_ok) last = (atomicAdd(tickets + sg, 1) == pieces - 1);
                 *last_flag = last;
             }
             named_barrier(1, C::CT);
@@ -574,6 +591,8 @@ decode_splitkv_kernel(const float* __restrict__ q, const float* __restrict__ k_c
             if (flat < r0 || flat >= r1) continue;
             const int64_t row = ((int64_t)kh * Lmax + L[m] - 1) * D;
             const int64_t nr = ((int64_t)m * Hk + kh) * D;
+            if (!in_bounds(row + D - 1, (int64_t)Hk * Lmax * D, flags) || !in_bounds(nr + D - 1, (int64_t)M * Hk * D, flags))
+                continue;
             for (int i = lane; i < D / 4; i += 32) {
                 reinterpret_cast<float4*>(const_cast<float*>(kbase[m]) + row)[i] =
                     __ldg(reinterpret_cast<const float4*>(k_new + nr) + i);

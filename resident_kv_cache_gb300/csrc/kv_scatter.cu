@@ -56,9 +56,12 @@ kv_scatter_kernel(const float4* __restrict__ k_new, const float4* __restrict__ v
         const int d4 = rem - kh * D4;
         const int64_t pos = (int64_t)p0 + t0 + j;
         if (pos < 0 || pos >= Lmax) continue;
+        const int64_t dst = ((int64_t)kh * Lmax + pos) * D4 + d4;
+        if (!in_bounds(src_base + idx, (int64_t)gridDim.y * T * row4, flags) ||
+            !in_bounds(dst, (int64_t)Hk * Lmax * D4, flags))
+            continue;
         const float4 kv = __ldcs(k_new + src_base + idx);
         const float4 vv = __ldcs(v_new + src_base + idx);
-        const int64_t dst = ((int64_t)kh * Lmax + pos) * D4 + d4;
         __stcs(kc + dst, kv);          // streaming stores: the cache is far larger than L2
         __stcs(vc + dst, vv);
     }
@@ -73,7 +76,7 @@ kv_scatter_kernel(const float4* __restrict__ k_new, const float4* __restrict__ v
 template <int D4>
 __global__ void __launch_bounds__(kScatterThreads)
 kv_fill_kernel(const float4* __restrict__ k, const float4* __restrict__ v, float4* __restrict__ k_cache,
-               float4* __restrict__ v_cache, int S, int Hk, int Lmax, int64_t total) {
+               float4* __restrict__ v_cache, int S, int Hk, int Lmax, int64_t total, unsigned int* __restrict__ flags) {
     const int row4 = Hk * D4;                         // float4 elements per token
 #pragma unroll 4
     for (int64_t idx = (int64_t)blockIdx.x * kScatterThreads + threadIdx.x; idx < total;
@@ -83,6 +86,7 @@ kv_fill_kernel(const float4* __restrict__ k, const float4* __restrict__ v, float
         const int kh = rem / D4, d4 = rem - kh * D4;
         const int64_t b = tok / S, t = tok - b * S;
         const int64_t dst = ((b * Hk + kh) * Lmax + t) * D4 + d4;
+        if (!in_bounds(dst, total / ((int64_t)S * row4) * Hk * Lmax * D4, flags)) continue;
         __stcs(k_cache + dst, __ldg(k + idx));
         __stcs(v_cache + dst, __ldg(v + idx));
     }
@@ -90,7 +94,7 @@ kv_fill_kernel(const float4* __restrict__ k, const float4* __restrict__ v, float
 }
 
 rkv_status launch_fill_dependent(const float* k, const float* v, float* k_cache, float* v_cache, int B, int S,
-                                 int Hk, int D, int Lmax, cudaStream_t stream) {
+                                 int Hk, int D, int Lmax, unsigned int* flags, cudaStream_t stream) {
     const int sms = sm_count();
     if (sms <= 0) return set_error(RKV_ERR_LAUNCH, "attn_prefill_fill_cache: cannot query the SM count");
     cudaLaunchConfig_t cfg = {};
@@ -110,10 +114,10 @@ rkv_status launch_fill_dependent(const float* k, const float* v, float* k_cache,
     auto vc = reinterpret_cast<float4*>(v_cache);
     cudaError_t e;
     switch (D) {
-        case 16: e = cudaLaunchKernelEx(&cfg, kv_fill_kernel<4>, k4, v4, kc, vc, S, Hk, Lmax, total); break;
-        case 32: e = cudaLaunchKernelEx(&cfg, kv_fill_kernel<8>, k4, v4, kc, vc, S, Hk, Lmax, total); break;
-        case 64: e = cudaLaunchKernelEx(&cfg, kv_fill_kernel<16>, k4, v4, kc, vc, S, Hk, Lmax, total); break;
-        case 128: e = cudaLaunchKernelEx(&cfg, kv_fill_kernel<32>, k4, v4, kc, vc, S, Hk, Lmax, total); break;
+        case 16: e = cudaLaunchKernelEx(&cfg, kv_fill_kernel<4>, k4, v4, kc, vc, S, Hk, Lmax, total, flags); break;
+        case 32: e = cudaLaunchKernelEx(&cfg, kv_fill_kernel<8>, k4, v4, kc, vc, S, Hk, Lmax, total, flags); break;
+        case 64: e = cudaLaunchKernelEx(&cfg, kv_fill_kernel<16>, k4, v4, kc, vc, S, Hk, Lmax, total, flags); break;
+        case 128: e = cudaLaunchKernelEx(&cfg, kv_fill_kernel<32>, k4, v4, kc, vc, S, Hk, Lmax, total, flags); break;
         default: return set_error(RKV_ERR_UNSUPPORTED, "attn_prefill_fill_cache: head_dim %d", D);
     }
     if (e != cudaSuccess)

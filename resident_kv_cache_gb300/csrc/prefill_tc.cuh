@@ -662,7 +662,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             const int qi = w.q0 + r;
             float4* op = reinterpret_cast<float4*>(o + ((int64_t)w.b * S + qi) * q_row + (int64_t)w.h * D);
             if (w.nblk == 0) {      // no key is visible to any row of this tile: padding -> zeros
-                if (qi < S) {
+                if (qi < S && in_bounds(((int64_t)w.b * S + qi) * q_row + (int64_t)w.h * D, (int64_t)B * S * q_row, flags)) {
 #pragma unroll
                     for (int e = 0; e < D / 4; ++e) __stcs(op + e, make_float4(0.f, 0.f, 0.f, 0.f));
                 }
@@ -943,7 +943,7 @@ rkv_status launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
         (int)n_work, kv, a.flags);
     if (check_launch(a.op) != RKV_OK) return RKV_ERR_LAUNCH;
     if (FILL) return launch_fill_dependent(a.k, a.v, a.k_cache_out, a.v_cache_out, a.B, a.S, a.Hk, D, a.fill_max_len,
-                                           stream);
+                                           a.flags, stream);
     return RKV_OK;
 }
 

@@ -23,6 +23,29 @@ int sm_count();   // SMs of the current device (cached per device)
 // ----------------------------------------------------------------- constants
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait, then abort
 
+// ------------------------------------------------------------- debug checks
+// The checked build (RKV_DEVICE_CHECKS=1, librkv_attn_checked.so) tests every index the kernels
+// compute for a plain global access or an untiled bulk copy against the extent of its buffer
+// before the access; an index outside raises RKV_FLAG_BOUNDS and the access is skipped (a device
+// assert would stop the GPU instead).  Tensor-map copies need no check: the copy engine clips
+// them to the map's extents.  In the release build in_bounds() is constant true and the checks
+// compile away.
+#ifndef RKV_DEVICE_CHECKS
+#define RKV_DEVICE_CHECKS 0
+#endif
+__device__ __forceinline__ bool in_bounds(int64_t i, int64_t n, unsigned int* flags) {
+#if RKV_DEVICE_CHECKS
+    if (i >= 0 && i < n) return true;
+    atomicOr(flags, RKV_FLAG_BOUNDS);
+    return false;
+#else
+    (void)i;
+    (void)n;
+    (void)flags;
+    return true;
+#endif
+}
+
 // --------------------------------------------------------------- small utils
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -75,6 +75,6 @@ rkv_status launch_rope_append(float* q, float* k_new, const float* v_new, float*
 // programmatic dependent of the kernel just enqueued on `stream`: it may start while that kernel
 // runs, and completes only after it.
 rkv_status launch_fill_dependent(const float* k, const float* v, float* k_cache, float* v_cache, int B, int S,
-                                 int Hk, int D, int Lmax, cudaStream_t stream);
+                                 int Hk, int D, int Lmax, unsigned int* flags, cudaStream_t stream);
 
 }  // namespace rkv

@@ -68,8 +68,10 @@ rope_append_kernel(float4* __restrict__ q, float4* __restrict__ k_new, const flo
             const int head = u / h4, c4 = u - head * h4;
             const bool is_q = head < H;
             const int hh = is_q ? head : head - H;
-            float4* row = is_q ? q + ((int64_t)m * T + t) * H * D4 + (int64_t)hh * D4
-                               : k_new + ((int64_t)m * T + t) * Hk * D4 + (int64_t)hh * D4;
+            const int64_t roff = is_q ? ((int64_t)m * T + t) * H * D4 + (int64_t)hh * D4
+                                      : ((int64_t)m * T + t) * Hk * D4 + (int64_t)hh * D4;
+            if (!in_bounds(roff + c4 + h4, (int64_t)gridDim.y * T * (is_q ? H : Hk) * D4, flags)) continue;
+            float4* row = (is_q ? q : k_new) + roff;
             const float4 x1 = row[c4], x2 = row[c4 + h4];
             const float2 a0 = cs[j][4 * c4], a1 = cs[j][4 * c4 + 1], a2 = cs[j][4 * c4 + 2], a3 = cs[j][4 * c4 + 3];
             const float4 y1 = make_float4(x1.x * a0.x - x2.x * a0.y, x1.y * a1.x - x2.y * a1.y,
@@ -78,7 +80,8 @@ rope_append_kernel(float4* __restrict__ q, float4* __restrict__ k_new, const flo
                                           x1.z * a2.y + x2.z * a2.x, x1.w * a3.y + x2.w * a3.x);
             row[c4] = y1;
             row[c4 + h4] = y2;
-            if (!is_q && in_cache) {
+            if (!is_q && in_cache &&
+                in_bounds((((int64_t)m * Hk + hh) * Lmax + pos) * D4 + c4 + h4, (int64_t)gridDim.y * Hk * Lmax * D4, flags)) {
                 float4* dst = k_cache + (((int64_t)m * Hk + hh) * Lmax + pos) * D4;
                 dst[c4] = y1;
                 dst[c4 + h4] = y2;
@@ -88,6 +91,9 @@ rope_append_kernel(float4* __restrict__ q, float4* __restrict__ k_new, const flo
             const int hh = u / D4, c4 = u - hh * D4;
             const int64_t src = ((int64_t)m * T + t) * Hk * D4 + (int64_t)hh * D4 + c4;
             const int64_t dst = (((int64_t)m * Hk + hh) * Lmax + pos) * D4 + c4;
+            if (!in_bounds(src, (int64_t)gridDim.y * T * Hk * D4, flags) ||
+                !in_bounds(dst, (int64_t)gridDim.y * Hk * Lmax * D4, flags))
+                continue;
             if (c4 >= 2 * h4) k_cache[dst] = k_new[src];   // tail of k (not rotated)
             v_cache[dst] = __ldg(v_new + src);
         }

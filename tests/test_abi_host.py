@@ -113,6 +113,22 @@ def test_decode_workspace_query(lib):
     assert binding.attn_decode_workspace_bytes(1, 8193, 8193, 16, 64) == 0
 
 
+def test_checked_build_exports_every_declared_function():
+    """The debug build with the device index checks compiled in (librkv_attn_checked.so)."""
+    path = build.build(checked=True)
+    lib = ctypes.CDLL(path)
+    for n in binding.declared_functions():
+        assert hasattr(lib, n), f"{n} missing from the checked build"
+
+
+def test_bounds_flag_matches_the_header():
+    import os
+    import re
+    hdr = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "rkv_attn.h")
+    m = re.search(r"#define\s+RKV_FLAG_BOUNDS\s+(0x[0-9a-fA-F]+)u", open(hdr).read())
+    assert m and int(m.group(1), 16) == binding.RKV_FLAG_BOUNDS
+
+
 def test_ticket_block_size_matches_the_header():
     import os
     import re
