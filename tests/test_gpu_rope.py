@@ -107,3 +107,35 @@ def test_prefill_with_rope_prologue(rkv, oracle_mod):
     want = oracle_mod.prefill(qr, kr, v, B, S, H, Hk, D, True)
     assert_close(o.cpu().numpy(), want, 3e-3, 1e-3, what="prefill with RoPE")
     assert np.array_equal(kc.cpu().numpy()[:, :, :S, :], dk.cpu().numpy().reshape(B, S, Hk, D).transpose(0, 2, 1, 3))
+
+
+def test_decode_step_with_rope_prologue_full_size(rkv, oracle_mod):
+    """The batched decode step with the RoPE prologue exactly as it is timed: the batched decode
+    workload's inputs (M=32, H=32, Hk=8, D=128, cache [32,8,4096,128], lengths U{1..4096}),
+    kv_append_rope at len-1 (theta 1e6, every dim rotated), then attn_decode_batched over len rows;
+    the whole output against the oracle and the caches bit for bit."""
+    torch = torch_cuda()
+    d = inputs.BATCHED_DECODE
+    x = inputs.batched_decode_inputs(d)
+    M, H, Hk, D, L = d.M, d.H, d.Hk, d.D, d.Lmax
+    dq = torch.from_numpy(x["q"]).cuda()
+    dk = torch.from_numpy(x["k_new"]).cuda()
+    dv = torch.from_numpy(x["v_new"]).cuda()
+    kc, vc = torch.from_numpy(x["k_cache"]).cuda(), torch.from_numpy(x["v_cache"]).cuda()
+    sp, ln = torch.from_numpy(x["start_pos"]).cuda(), torch.from_numpy(x["lens"]).cuda()
+    rkv.kv_append_rope(dq, dk, dv, kc, vc, M, 1, H, Hk, D, L, sp, theta=1e6)
+    n = rkv.attn_decode_workspace_bytes(M, H, Hk, D, L)
+    ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    o = torch.full((M, H * D), float("nan"), device="cuda")
+    rkv.attn_decode_batched(dq, kc, vc, o, M, H, Hk, D, L, ln, 0.0, ws, n)
+    torch.cuda.synchronize()
+    pos = x["start_pos"]
+    qr = oracle_mod.rope(x["q"], H, D, pos, theta=1e6).astype(np.float32)
+    kr = oracle_mod.rope(x["k_new"].reshape(M, Hk * D), Hk, D, pos, theta=1e6).astype(np.float32)
+    assert np.abs(dq.cpu().numpy() - qr).max() <= 1e-5
+    # the cache receives exactly the rotated k the call left in k_new
+    hk, hv, _ = oracle_mod.scatter(dk.cpu().numpy(), x["v_new"], x["k_cache"], x["v_cache"], M, 1, Hk, D, L, pos)
+    assert np.array_equal(kc.cpu().numpy(), hk) and np.array_equal(vc.cpu().numpy(), hv)
+    assert np.abs(dk.cpu().numpy().reshape(M, Hk * D) - kr).max() <= 1e-5
+    want = oracle_mod.decode(qr, hk, hv, M, H, Hk, D, L, x["lens"])
+    assert_close(o.cpu().numpy(), want, 1e-4, what="decode step with RoPE, full size")
