@@ -222,6 +222,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     }
 
     // ------------------------------------------------------------------ setup
+    // Thread 0 initialises the barriers and is also the K producer: it issues the first item's
+    // query tile and first key tiles straight away (the barriers are fresh, no slot to wait
+    // for), so they are in flight while tensor memory is allocated and the CTA synchronises.
+    int k_first = -1, k_pre = 0;                   // (thread 0) that item and its fills issued
     if (warp == 1) {
         tmem_alloc(smem_addr(tmem_slot), kPfTmemCols);
         tmem_relinquish();
@@ -253,6 +257,28 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_o);
+        for (int k = 0;; ++k) {
+            const int u = pf_item(k);
+            if (u >= n_work) break;
+            const PfWork w = work(u);
+            if (w.nblk == 0) continue;
+            k_first = k;
+            k_pre = min(C::NK, C::QSLOTS + w.nblk);
+            for (int f = 0; f < k_pre; ++f) {          // fill f of the ring: query tile, then keys
+                const uint32_t full = bar.k_full + 8 * f;
+                mbar_arrive_expect_tx(full, C::TILE);
+                const int j = f - C::QSLOTS;
+                const bool qfill = j < 0;
+                const void* map = qfill ? static_cast<const void*>(&tm_q) : static_cast<const void*>(&tm_k);
+                const int x0 = qfill ? w.h * D : w.g * kv.xg;
+                const int y0 = qfill ? w.q0 + f * BN : j * BN;
+                const int z0 = qfill ? w.b : w.b * kv.zb + w.g * kv.zg;
+#pragma unroll
+                for (int c = 0; c < C::NCH; ++c)
+                    tma_load_3d(smem_addr(smem + C::OFF_K) + C::koff(f, c), map, x0 + c * C::CH, y0, z0, full);
+            }
+            break;
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -268,7 +294,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         // With paired slots the query fills must start on an even fill; an empty pad fill (a
         // plain arrival, no data) restores that after an odd block count.
         if (lane == 0) {
-            int gs = 0;                   // fills of the K ring so far
+            int gs = k_pre;               // fills of the K ring so far (the first ones issued at setup)
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int u = pf_item(k);
@@ -286,9 +312,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                                 tma_prefetch_l2_3d(&tm_q, wn.h * D + c * C::CH, wn.q0 + i * BN, wn.b);
                     }
                 }
-                const bool pad = C::KPAIR && (gs & 1);
+                const bool first = k == k_first;
+                const bool pad = !first && C::KPAIR && (gs & 1);
                 constexpr int nq = C::QSLOTS;
-                for (int j = -nq - (pad ? 1 : 0); j < w.nblk; ++j) {
+                for (int j = first ? k_pre - nq : -nq - (pad ? 1 : 0); j < w.nblk; ++j) {
                     const int s = gs % C::NK;
                     if (!(ok = mbar_wait(bar.k_empty + 8 * s, ((uint32_t)(gs / C::NK) & 1u) ^ 1u, abort_flag, flags)))
                         break;
