@@ -13,7 +13,10 @@ rkv_status launch_prefill_guarded(const PrefillArgs& a, cudaStream_t stream);   
 
 rkv_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     // per-sequence lengths or keys from the cache: tiles may reach past a sequence
-    if (a.kv_cache || a.seq_lens) return launch_prefill_guarded(a, stream);
+    const bool guard = a.kv_cache || a.seq_lens;
+    // head_dim 128 with pairs of query heads per kv head: two CTAs share each product
+    if (prefill_pair_supported(a)) return launch_prefill_pair(a, guard, stream);
+    if (guard) return launch_prefill_guarded(a, stream);
     if (a.k_cache_out) {                // whole sequences, their K/V also written to the cache
         switch (a.D) {
             case 16: return launch_prefill_tc_t<16, false, true>(a, stream);

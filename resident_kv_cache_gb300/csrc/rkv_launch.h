@@ -54,6 +54,10 @@ struct DecodeArgs {
 };
 
 rkv_status launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+// The CTA-pair prefill (prefill_pair.cu): head_dim 128 and an even number of query heads per kv
+// head.
+bool prefill_pair_supported(const PrefillArgs& a);
+rkv_status launch_prefill_pair(const PrefillArgs& a, bool guard, cudaStream_t stream);
 
 bool decode_group_supported(int group);
 size_t decode_workspace_bytes(int M, int H, int Hk, int D);
