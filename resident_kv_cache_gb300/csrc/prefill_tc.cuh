@@ -405,10 +405,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         }
     } else if (warp == 1 || warp == kPfPvWarp) {
         // ================================================================ MMA issuers
-        // Two threads issue: warp 1 the QK^T MMAs, warp 10 the PV MMAs.  A thread needs
-        // ~45 cycles per tcgen05.mma it issues, more than one N=64 MMA takes to run,
-        // so a single issuer would starve the tensor core.
-        if (lane == 0) {
+        // Two warps issue: warp 1 the QK^T MMAs, warp 10 the PV MMAs.  Each walks its loop as a
+        // whole warp (every value in it is warp-uniform), waits are decided by the warp together,
+        // one elected lane executes each MMA and commit, and lane 0 makes the plain arrivals.
+        {
             const bool qk_role = warp == 1;
             constexpr uint32_t id_qk = idesc_tf32(kPfBM, BN, false);
             constexpr uint32_t id_qk2 = idesc_tf32(kPfBM, 2 * BN, false);
@@ -430,19 +430,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 if (qk_role) {
                     // K-ring fills of this item: [pad] query tile (QSLOTS) then one per key block
                     if (C::KPAIR && (f & 1)) {      // pad fill: nothing to read, hand it back
-                        if (!(ok = mbar_wait(bar.k_full + 8 * (f % C::NK), (uint32_t)(f / C::NK) & 1u, abort_flag,
-                                             flags)))
-                            break;
-                        mbar_arrive(bar.k_empty + 8 * (f % C::NK));
+                        ok = mbar_wait(bar.k_full + 8 * (f % C::NK), (uint32_t)(f / C::NK) & 1u, abort_flag, flags);
+                        if (!(ok = __all_sync(0xffffffffu, ok))) break;
+                        if (lane == 0) mbar_arrive(bar.k_empty + 8 * (f % C::NK));
                         ++f;
                     }
                     // The Q/V^T warps read the item's query tile out of the K ring, round it and
                     // write it into TMEM columns kColQ.. (after the previous item's QK^T MMAs,
                     // committed to q_free, are done reading them).  Once they have, the query
                     // slots are handed back to the K producer.
-                    if (!(ok = mbar_wait(bar.q_ready, (uint32_t)t & 1u, abort_flag, flags))) break;
+                    ok = mbar_wait(bar.q_ready, (uint32_t)t & 1u, abort_flag, flags);
+                    if (!(ok = __all_sync(0xffffffffu, ok))) break;
                     tc_fence_after();
-                    for (int i = 0; i < C::QSLOTS; ++i) mbar_arrive(bar.k_empty + 8 * ((f + i) % C::NK));
+                    if (lane == 0)
+                        for (int i = 0; i < C::QSLOTS; ++i) mbar_arrive(bar.k_empty + 8 * ((f + i) % C::NK));
                     f += C::QSLOTS;
                     // S of block gb goes to buffer gb % NSBUF.  Paired blocks (D = 128: fill f
                     // even, adjacent buffers) share one N = 2*BN chain.  Before QK overwrites a
@@ -461,7 +462,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                                 ok = mbar_wait(bar.k_full + 8 * ((fb + i) % C::NK), (uint32_t)((fb + i) / C::NK) & 1u,
                                                abort_flag, flags);
                         }
-                        if (!ok) break;
+                        if (!(ok = __all_sync(0xffffffffu, ok))) break;
                         tc_fence_after();
                         const int s = fb % C::NK;
                         const uint32_t d_tmem = tmem + kColS + (uint32_t)((gb % C::NSBUF) * C::S_BUF);
@@ -484,14 +485,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     // O is reused item after item: PV of a new item starts (accumulate = 0)
                     // only after the epilogue has read the previous item's O.
                     if (t > 0) ok = mbar_wait(bar.o_free, (uint32_t)(t - 1) & 1u, abort_flag, flags);
+                    ok = __all_sync(0xffffffffu, ok);
                     for (int j = 0; ok && j < w.nblk; ++j) {
                         // O += P_gb V_gb
                         const int gb = g0 + j, vf = fv + j;
                         const int sv = vf % C::NV, sb = gb % C::NSBUF;
-                        if (!(ok = mbar_wait(bar.p_ready + 8 * sb, (uint32_t)(gb / C::NSBUF) & 1u, abort_flag, flags)))
-                            break;
-                        if (!(ok = mbar_wait(bar.v_full + 8 * sv, (uint32_t)(vf / C::NV) & 1u, abort_flag, flags)))
-                            break;
+                        ok = mbar_wait(bar.p_ready + 8 * sb, (uint32_t)(gb / C::NSBUF) & 1u, abort_flag, flags);
+                        if (ok) ok = mbar_wait(bar.v_full + 8 * sv, (uint32_t)(vf / C::NV) & 1u, abort_flag, flags);
+                        if (!(ok = __all_sync(0xffffffffu, ok))) break;
                         tc_fence_after();
                         const uint64_t vd = vdesc0 + (uint64_t)(sv * (C::TILE >> 4));
                         const uint32_t a_tmem = tmem + kColS + (uint32_t)(sb * C::S_BUF);
@@ -703,28 +704,31 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 if (!(ok = __all_sync(0xffffffffu, ok))) break;   // warp-uniform before TMEM access
                 tc_fence_after();
                 const uint32_t s_col = lane_base + kColS + (uint32_t)((gb % C::NSBUF) * C::S_BUF);
-                float s[BN];
-                {   // all chunks of the row in flight before one wait
-                    uint32_t wv[BN];
-#pragma unroll
-                    for (int c = 0; c < BN / 32; ++c)
-                        tmem_ld32(s_col + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(wv + 32 * c));
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < BN; ++e) s[e] = __uint_as_float(wv[e]);
-                }
+                // S is read out of TMEM twice in 32-column chunks, with the chunk loops rolled: the
+                // code stays small (fewer instruction-cache misses) and no more than one chunk of
+                // scores is live at a time.
                 const int k0 = j * BN;
                 const int nvis = min(max(key_lim - k0, 0), BN);     // visible keys of this block
-                if (__any_sync(0xffffffffu, nvis < BN)) {
-#pragma unroll
-                    for (int e = 0; e < BN; ++e)
-                        if (e >= nvis) s[e] = -INFINITY;
-                }
+                const bool masked = __any_sync(0xffffffffu, nvis < BN);
+                // pass 1: the block's row maximum (columns past nvis left out)
                 float mx[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) mx[e] = s[e];
+                for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t wv[32];
+                    tmem_ld32(s_col + 32 * c, wv);
+                    tmem_wait_ld();
+                    if (masked) {
+                        const int lim = nvis - 32 * c;
 #pragma unroll
-                for (int e = 8; e < BN; ++e) mx[e & 7] = fmaxf(mx[e & 7], s[e]);
+                        for (int e = 0; e < 32; ++e)
+                            mx[e & 7] = fmaxf(mx[e & 7], e < lim ? __uint_as_float(wv[e]) : -INFINITY);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(wv[e]));
+                    }
+                }
                 // S holds raw q.k; scores in the exponent's units are s * scale*log2(e) (> 0,
                 // so the maximum commutes with the scaling)
                 const float m_blk = scale_log2 * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
@@ -733,48 +737,38 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const bool need = m_blk > m_run + kLazyRescale;
                 const float m_use = need ? m_blk : m_run;
                 const float alpha = need ? fast_exp2(m_run - m_blk) : 1.0f;
-                // p = 2^(s*c - m); the tensor core truncates f32 operands to TF32, so p is
-                // truncated here too and the row sum is taken over exactly those values, in eight
-                // partial sums (column e into sum e & 7).
-                float ls[8];
-                if constexpr (BN == 64) {
-                    // Columns in pairs through the packed f32x2 FMA and add: the same per-lane
-                    // roundings as the scalar loop below, half the instructions on the softmax's
-                    // critical path (packed sum k holds partial sums 2k and 2k+1).
-                    uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
-                    const uint64_t sl2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-m_use, -m_use);
+                // pass 2: p = 2^(s*c - m); the tensor core truncates f32 operands to TF32, so p is
+                // truncated here too and written back over S, and the row sum is taken over exactly
+                // those values in eight partial sums (column e into sum e & 7), two columns at a time
+                // through the packed f32x2 FMA and add (each lane rounded as the scalar operation;
+                // packed sum k holds partial sums 2k and 2k+1).
+                uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
+                const uint64_t sl2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-m_use, -m_use);
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t wv[32];
+                    tmem_ld32(s_col + 32 * c, wv);
+                    tmem_wait_ld();
+                    if (masked) {
+                        const int lim = nvis - 32 * c;
 #pragma unroll
-                    for (int c = 0; c < BN / 32; ++c) {
-                        uint32_t wv[32];
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            float t0, t1;
-                            f2_unpack(f2_fma(f2_pack(s[32 * c + e], s[32 * c + e + 1]), sl2, nm2), t0, t1);
-                            wv[e] = __float_as_uint(fast_exp2(t0)) & 0xFFFFE000u;   // 2^-inf = +0 when masked
-                            wv[e + 1] = __float_as_uint(fast_exp2(t1)) & 0xFFFFE000u;
-                            ls2[(e & 7) >> 1] =
-                                f2_add(ls2[(e & 7) >> 1], f2_pack(__uint_as_float(wv[e]), __uint_as_float(wv[e + 1])));
-                        }
-                        tmem_st32(s_col + 32 * c, wv);
+                        for (int e = 0; e < 32; ++e)
+                            if (e >= lim) wv[e] = __float_as_uint(-INFINITY);     // 2^-inf = +0
                     }
 #pragma unroll
-                    for (int k2 = 0; k2 < 4; ++k2) f2_unpack(ls2[k2], ls[2 * k2], ls[2 * k2 + 1]);
-                } else {   // BN = 128: all 128 scores are live; the packed form would spill here
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) ls[e] = 0.f;
-#pragma unroll
-                    for (int c = 0; c < BN / 32; ++c) {
-                        uint32_t wv[32];
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const float x = s[32 * c + e];
-                            const float p = fast_exp2(fmaf(x, scale_log2, -m_use));   // 2^-inf = +0 when masked
-                            wv[e] = __float_as_uint(p) & 0xFFFFE000u;
-                            ls[e & 7] += __uint_as_float(wv[e]);
-                        }
-                        tmem_st32(s_col + 32 * c, wv);
+                    for (int e = 0; e < 32; e += 2) {
+                        float t0, t1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(wv[e]), __uint_as_float(wv[e + 1])), sl2, nm2), t0, t1);
+                        wv[e] = __float_as_uint(fast_exp2(t0)) & 0xFFFFE000u;
+                        wv[e + 1] = __float_as_uint(fast_exp2(t1)) & 0xFFFFE000u;
+                        ls2[(e & 7) >> 1] =
+                            f2_add(ls2[(e & 7) >> 1], f2_pack(__uint_as_float(wv[e]), __uint_as_float(wv[e + 1])));
                     }
+                    tmem_st32(s_col + 32 * c, wv);
                 }
+                float ls[8];
+#pragma unroll
+                for (int k2 = 0; k2 < 4; ++k2) f2_unpack(ls2[k2], ls[2 * k2], ls[2 * k2 + 1]);
                 const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
                 l_run = l_run * alpha + lsum;
                 m_run = m_use;

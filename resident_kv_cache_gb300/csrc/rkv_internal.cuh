@@ -271,20 +271,28 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool b_mn_major)
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[tmem] * B[smem desc]   (kind::tf32, one CTA)
+// MMAs and commits are issued by a whole converged warp, with elect.sync picking one lane (the
+// lowest, the same every time) to execute them: operands that are uniform across the warp then
+// stay in uniform registers, and an MMA issues in 32 cycles where a single-lane loop needs about
+// 49 (measured with N = 64 chains).  A commit tracks the MMAs of the lane that executes it, which
+// is the elected one throughout.
+
+// D[tmem] (+)= A[tmem] * B[smem desc]   (kind::tf32, one CTA); call from a whole warp
 __device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
-// Arrive on an mbarrier once every tcgen05 op issued so far by this thread completes.
+// Arrive on an mbarrier once every tcgen05 op issued so far by the elected lane completes; call
+// from a whole warp.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
         : "memory");
 }
 
@@ -348,11 +356,8 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
         : "memory");
 }
 
-// The pair's MMAs and commits are issued by a whole converged warp, with elect.sync picking one
-// lane (the lowest, the same every time) to execute them: operands that are uniform across the
-// warp then stay in uniform registers, and an MMA issues in about two thirds of the time a
-// single-lane loop takes.  A commit tracks the MMAs of the lane that executes it, which is the
-// elected one throughout.
+// The pair's MMAs and commits are issued like mma_tf32_ts / mma_commit: by a whole warp, one
+// elected lane executing them.
 
 // D[tmem] (+)= A[smem desc] * B[smem desc], M = 256 over the pair (kind::tf32); call from a whole warp
 __device__ __forceinline__ void mma_tf32_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
