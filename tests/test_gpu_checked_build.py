@@ -114,6 +114,29 @@ torch.cuda.synchronize()
 want = oracle.prefill_cached(qc, kcache.cpu().numpy(), vcache.cpu().numpy(), B, 20, H, Hk, D, L, True, p0)
 assert_close(oc.cpu().numpy(), want, 3e-3, 1e-3)
 bounds_clear("attn_prefill_chunked")
+
+# the same three at head_dim 128 with pairs of query heads per kv head (the CTA-pair kernel)
+B, S, H, Hk, D = 3, 130, 4, 2, 128
+q, k, v = (inputs.normal((B, S, n * D), (74, i)) for i, n in enumerate((H, Hk, Hk)))
+o = torch.full((B, S, H * D), float("nan"), device=dev)
+rkv.attn_prefill(to(q), to(k), to(v), o, B, S, H, Hk, D, True, to(sl))
+torch.cuda.synchronize()
+assert_close(o.cpu().numpy(), oracle.prefill(q, k, v, B, S, H, Hk, D, True, seq_lens=sl), 3e-3, 1e-3)
+bounds_clear("attn_prefill (pair)")
+kcache, vcache = torch.zeros((B, Hk, L, D), device=dev), torch.zeros((B, Hk, L, D), device=dev)
+o2 = torch.empty((B, S, H * D), device=dev)
+rkv.attn_prefill_fill_cache(to(q), to(k), to(v), o2, B, S, H, Hk, D, True, kcache, vcache, L)
+torch.cuda.synchronize()
+assert np.array_equal(kcache[:, :, :S].cpu().numpy(), k.reshape(B, S, Hk, D).transpose(0, 2, 1, 3))
+assert_close(o2.cpu().numpy(), oracle.prefill(q, k, v, B, S, H, Hk, D, True), 3e-3, 1e-3)
+bounds_clear("attn_prefill_fill_cache (pair)")
+qc = inputs.normal((B, 20, H * D), (74, 9))
+oc = torch.empty((B, 20, H * D), device=dev)
+rkv.attn_prefill_chunked(to(qc), kcache, vcache, oc, B, 20, H, Hk, D, L, True, to(p0))
+torch.cuda.synchronize()
+want = oracle.prefill_cached(qc, kcache.cpu().numpy(), vcache.cpu().numpy(), B, 20, H, Hk, D, L, True, p0)
+assert_close(oc.cpu().numpy(), want, 3e-3, 1e-3)
+bounds_clear("attn_prefill_chunked (pair)")
 print("CHECKED BUILD OK")
 '''
 
