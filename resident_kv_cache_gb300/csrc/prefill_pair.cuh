@@ -375,11 +375,10 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     } else if (warp >= kPfVWarp0 && warp < kPfVWarp0 + 4) {
         // ================================================================ Q and V^T
         // Each thread rounds its query row of the Q buffer to nearest TF32 in place (its eight
-        // 16-byte chunks at their swizzled places, so a quarter-warp touches eight distinct
-        // banks).  Each V half
-        // arrives as 2 d chunks x 128 key rows (swizzled like K) and is rewritten in place as
-        // V^T: 4 key chunks x 64 d rows, with the diagonal 4x4-block map of prefill_tc.cuh, which
-        // keeps both the 16-byte loads and the 16-byte stores free of bank conflicts.
+        // 16-byte chunks at their swizzled places, so a quarter-warp touches eight distinct banks).
+        // Each V half arrives as 2 d chunks x 128 key rows (swizzled like K) and is rewritten in
+        // place as V^T: 4 key chunks x 64 d rows, with the diagonal 4x4-block map of prefill_tc.cuh,
+        // which keeps both the 16-byte loads and the 16-byte stores free of bank conflicts.
         const int wv = warp - kPfVWarp0;                      // 0..3
         constexpr int DH = D / 2;                             // this CTA's d columns of V
         constexpr int PER = (BN / 4) * (DH / 4) / 128;        // 4x4 blocks per thread per tile
