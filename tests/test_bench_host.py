@@ -33,3 +33,29 @@ def test_nominal_fraction_beside_each_roofline():
     r = bench.with_nominal({"unit": "TFLOP/s", "value": 550.0})
     assert r["nominal"]["peak"] == 1100.0 and abs(r["nominal"]["frac"] - 0.5) < 1e-12
     assert "nominal" not in bench.with_nominal({"unit": "us", "value": 3.0})
+
+
+def test_traffic_figures_are_keyed_to_every_source_of_their_kernel():
+    """bench.py reports an ncu DRAM figure only while the source hash it was taken on matches:
+    the hashed file set of each kernel must exist and take in every source its launch compiles
+    (both prefill kernels, which share one launch path), or a changed kernel would keep a stale
+    figure."""
+    import glob
+    import json
+    import os
+    csrc = os.path.join(bench.ROOT, "resident_kv_cache_gb300", "csrc")
+    for kernel, files in bench.KERNEL_FILES.items():
+        for f in files:
+            assert os.path.exists(os.path.join(csrc, f)), (kernel, f)
+    prefill_sources = {os.path.basename(p) for p in glob.glob(os.path.join(csrc, "prefill_*"))
+                       if not os.path.basename(p).endswith("_guarded.cu")}
+    assert prefill_sources <= set(bench.KERNEL_FILES["prefill"])
+    assert "rkv_internal.cuh" in bench.KERNEL_FILES["prefill"]
+    assert "decode_splitkv.cu" in bench.KERNEL_FILES["decode"]
+    with open(os.path.join(bench.ROOT, "profiles", "ncu_traffic.json")) as fh:
+        table = json.load(fh)
+    for kernel, entry in table.items():
+        assert kernel in bench.KERNEL_FILES
+        h = entry["source_hash"]
+        assert len(h) == 16 and all(c in "0123456789abcdef" for c in h)
+        assert entry["dram_bytes_per_launch"] > 0
